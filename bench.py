@@ -1,0 +1,455 @@
+"""Benchmark of the GB300 sparse-MoE expert path (one JSON line on rank 0).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path (route -> grouped FFN -> combine) over one batch of
+synthetic input of the workload.  Default workload: the 512-token prefill chunk (T=512, d=2048,
+256 experts, top-8, I=512 + shared expert), whose 455 MB of 4-bit weights exceed L2, so every
+step streams its inputs from HBM.  Timing: W untimed steps, then K steps between CUDA events on
+the launching stream (each step is replayed from CUDA graphs of the library calls), barrier +
+synchronize on both sides, max over ranks.  Multi-GPU (torchrun): every rank runs its own
+chunks (weak scaling, no collective on the data path).
+
+--impl reference times the CPU oracle (the reference of this build) on bounded samples of the
+same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer routed tokens/s (prefill) & decode µs/token; % of TC/HBM roofline"
+DEFAULT_WORKLOAD = "prefill_t512_d2048"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=32)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "50"], stdout=open(self.out, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.out):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), active=f[4], hw=f[5], hwt=f[6], swt=f[7], pcap=f[8]))
+            except ValueError:
+                continue
+        try:
+            os.remove(self.out)
+        except OSError:
+            pass
+        if not rows:
+            return {"samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([r["sm"] for r in rows])), "sm_max_mhz": rows[0]["smax"],
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------- work
+def algorithmic_counts(shp, counts):
+    """Per-launch algorithmic bytes and FLOPs of the gate/up and down kernels (real rows only)."""
+    T, d, I = shp.T, shp.d, shp.I
+    touched = int((counts > 0).sum()) + 1                       # + the shared expert
+    q4 = lambda rows, cols: rows * cols // 2 + rows * (cols // 64) * 4   # codes + bf16 scale/bias
+    gu_w = touched * 2 * q4(I, d)
+    dn_w = touched * q4(d, I)
+    rows = 9 * T                                                # routed assignments + shared rows
+    gu_bytes = gu_w + rows * d * 2 + rows * 2 * I * 2           # weights + activation rows + h (hi|lo)
+    dn_bytes = dn_w + rows * 2 * I * 2 + T * d * 4 * 2          # weights + h + fp32 sum (read+write)
+    gu_flops = 2.0 * rows * d * 2 * I
+    dn_flops = 2.0 * rows * I * d
+    return dict(gu_bytes=gu_bytes, dn_bytes=dn_bytes, gu_flops=gu_flops, dn_flops=dn_flops,
+                weights_bytes=gu_w + dn_w, touched=touched)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import quantized_grouped_gemm_gb300 as moe
+    from moe_workload import configs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = configs.WORKLOADS[args.workload]
+    sh = wl.shape
+    decode = sh.T == 1
+    T = wl.chunk or sh.T
+    layers = wl.layers if decode else 1
+    shp = moe.shape(T, sh.d, sh.E, sh.k, sh.I, sh.I_shared)
+
+    def to_dev(a):
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a)).to(dev)
+
+    # weights: one layer (prefill) or `layers` independent copies (decode)
+    L = []
+    for li in range(layers):
+        lay = configs.make_layer(wl, layer=li)
+        q = lambda m: (to_dev(m.codes), to_dev(m.scales), to_dev(m.biases))
+        pr = moe.moe_pack_weights(shp, q(lay.routed.gate), q(lay.routed.up), q(lay.routed.down), sh.I)
+        ps = moe.moe_pack_weights(shp, q(lay.shared.gate), q(lay.shared.up), q(lay.shared.down), sh.I_shared)
+        torch.cuda.synchronize()
+        L.append(dict(wr=to_dev(lay.w_router), bias=None if lay.logit_bias is None else to_dev(lay.logit_bias),
+                      pr=pr, ps=ps))
+        del lay
+    # activations: prefill chunks of this rank, or decode steps
+    if decode:
+        nsteps_x = 1000
+        x_all = to_dev(configs.make_decode_x(wl, nsteps_x))
+    else:
+        x_full = configs.make_x(wl)
+        nchunk = sh.T // T
+        xs = [to_dev(np.ascontiguousarray(x_full[c * T:(c + 1) * T])) for c in range(nchunk)]
+        del x_full
+        if world > 1:      # weak scaling: each rank its own rotation of the chunks
+            xs = xs[rank % len(xs):] + xs[:rank % len(xs)]
+    rt = moe.Routing(T)
+    ws = moe.workspace(shp)
+    y = torch.empty(T, sh.d, dtype=torch.int16, device=dev)
+    x_in = torch.empty(T, sh.d, dtype=torch.int16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    opts = moe.options()
+
+    # ---- capture one step as graphs (per phase for prefill, all layers for decode)
+    n0 = moe.moe_launch_count()
+    graphs = {}
+    with torch.cuda.stream(stream):
+        if decode:
+            g = torch.cuda.CUDAGraph()
+            for li in range(layers):   # warm the kernels once outside capture
+                moe.moe_forward(shp, x_in, L[li]["wr"], L[li]["bias"], L[li]["pr"], L[li]["ps"], rt, ws, y, opts,
+                                stream)
+            stream.synchronize()
+            n0 = moe.moe_launch_count()
+            with torch.cuda.graph(g, stream=stream):
+                for li in range(layers):
+                    moe.moe_forward(shp, x_in, L[li]["wr"], L[li]["bias"], L[li]["pr"], L[li]["ps"], rt, ws, y, opts,
+                                    stream)
+            graphs["step"] = g
+        else:
+            l0 = L[0]
+            calls = {
+                "route": lambda: moe.moe_route(shp, x_in, l0["wr"], l0["bias"], rt, ws, opts, stream),
+                "gate_up": lambda: moe.moe_ffn_gate_up(shp, x_in, rt, l0["pr"], l0["ps"], ws, opts, stream),
+                "down": lambda: moe.moe_ffn_down(shp, rt, l0["pr"], l0["ps"], ws, opts, stream),
+                "combine": lambda: moe.moe_combine(shp, rt, ws, y, opts, stream),
+            }
+            x_in.copy_(xs[0])
+            for f in calls.values():
+                f()
+            stream.synchronize()
+            n0 = moe.moe_launch_count()
+            for name, f in calls.items():
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    f()
+                graphs[name] = g
+    launches_per_step = moe.moe_launch_count() - n0
+    torch.cuda.synchronize()
+
+    # per-chunk inputs: prefill graphs read x_in; a step copies its chunk into x_in first
+    # (device-to-device, T*d*2 bytes) -- part of the step for both the graph and eager paths
+    def step(s, ev=None):
+        if decode:
+            x_in.copy_(x_all[s % nsteps_x:s % nsteps_x + 1], non_blocking=True)
+            graphs["step"].replay()
+        else:
+            x_in.copy_(xs[s % len(xs)], non_blocking=True)
+            graphs["route"].replay()
+            if ev is not None:
+                ev[0].record(stream)
+            graphs["gate_up"].replay()
+            if ev is not None:
+                ev[1].record(stream)
+            graphs["down"].replay()
+            if ev is not None:
+                ev[2].record(stream)
+            graphs["combine"].replay()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            step(s)
+        stream.synchronize()
+        # auto step count: about 1.5 s of timed work
+        if args.steps is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for s in range(20):
+                step(s)
+            e1.record(stream)
+            e1.synchronize()
+            per = e0.elapsed_time(e1) / 20
+            K = int(min(20000, max(20, 1500.0 / max(per, 1e-3))))
+        else:
+            K = args.steps
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)] if not decode else None
+        clocks = ClockSampler(local)
+        clocks.start()
+        time.sleep(0.15)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for s in range(K):
+            step(s, evs[s] if evs else None)
+        t1.record(stream)
+        t1.synchronize()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    if dist is not None:
+        tt = torch.tensor([ms_total], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / K
+    rc, bits = moe.moe_read_status(ws, stream)
+    assert rc == moe.MOE_OK, f"device status {rc} bits {bits}"
+
+    P = peaks()
+    res = dict(metric=METRIC, n_gpus=world, steps=K, warmup=args.warmup, ms_per_step=ms_step, data="synthetic",
+               scaling="weak", vs_baseline=None, dtype="bf16", clocks=clk,
+               gpu_launches=int(launches_per_step * K))
+    if decode:
+        us_tok_layer = ms_step * 1000.0 / layers
+        res.update(value=us_tok_layer, unit="us/token/layer", higher_is_better=False)
+        bytes_layer = (sh.E * sh.d * 2) + 9 * 3 * (sh.d * sh.I // 2 + sh.d * (sh.I // 64) * 4 * (1 if True else 1))
+        bytes_layer = sh.E * sh.d * 2 + 9 * (3 * sh.d * sh.I // 2 + 3 * sh.d * sh.I // 64 * 4)
+        gbs = bytes_layer / (us_tok_layer * 1e-6) / 1e9
+        res["roofline"] = dict(bound="hbm", achieved=gbs, peak=P["hbm_gbs"], unit="GB/s", frac=gbs / P["hbm_gbs"],
+                               traffic=None, kernel="whole decode layer (route + gate/up GEMV + down GEMV)",
+                               bytes_per_token_layer=bytes_layer, peak_source=P["source"])
+        res["config"] = dict(workload=wl.name, T=1, d=sh.d, E=sh.E, k=sh.k, I=sh.I, I_shared=sh.I_shared,
+                             layers=layers, l2="inputs larger than L2: 40 layer copies of the weights, 18 GB",
+                             parallelism=f"replicas x{world}")
+    else:
+        value = world * T * K / (ms_total / 1000.0)
+        res.update(value=value, unit="routed tokens/s", higher_is_better=True)
+        ph = np.array([[evs[s][0].elapsed_time(evs[s][1]), evs[s][1].elapsed_time(evs[s][2])] for s in range(K)])
+        gu_ms, dn_ms = float(ph[:, 0].mean()), float(ph[:, 1].mean())
+        counts = rt.counts.cpu().numpy()
+        A = algorithmic_counts(shp, counts)
+        # dominant kernel: gate/up. Bound: HBM when its arithmetic intensity is below the ridge
+        ai = A["gu_flops"] / A["gu_bytes"]
+        ridge = P["bf16_tflops"] * 1e12 / (P["hbm_gbs"] * 1e9)
+        if ai < ridge:
+            ach = A["gu_bytes"] / (gu_ms * 1e-3) / 1e9
+            roof = dict(bound="hbm", achieved=ach, peak=P["hbm_gbs"], unit="GB/s", frac=ach / P["hbm_gbs"])
+        else:
+            ach = A["gu_flops"] / (gu_ms * 1e-3) / 1e12
+            roof = dict(bound="tensor", achieved=ach, peak=P["bf16_tflops"], unit="TFLOP/s", frac=ach / P["bf16_tflops"])
+        roof.update(traffic=None, kernel="ffn_gate_up_kernel", algorithmic_bytes=A["gu_bytes"],
+                    algorithmic_flops=A["gu_flops"], kernel_ms=gu_ms, peak_source=P["source"])
+        res["roofline"] = roof
+        ffn_ms = gu_ms + dn_ms
+        res["ffn"] = dict(gate_up_ms=gu_ms, down_ms=dn_ms, ffn_tflops=(A["gu_flops"] + A["dn_flops"]) / (ffn_ms * 1e-3) / 1e12,
+                          ffn_frac_bf16_peak=(A["gu_flops"] + A["dn_flops"]) / (ffn_ms * 1e-3) / 1e12 / P["bf16_tflops"],
+                          ffn_weight_gbs=A["weights_bytes"] / (ffn_ms * 1e-3) / 1e9,
+                          experts_touched=A["touched"], other_ms=ms_step - ffn_ms)
+        res["config"] = dict(workload=wl.name, T=T, d=sh.d, E=sh.E, k=sh.k, I=sh.I, I_shared=sh.I_shared,
+                             chunks=sh.T // T, l2="inputs larger than L2: 455 MB of 4-bit weights per step",
+                             parallelism=f"replicas x{world}")
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    if not decode:
+        xh = [t.cpu().pin_memory() for t in xs[:4]]
+        yh = torch.empty(T, sh.d, dtype=torch.int16).pin_memory()
+        l0 = L[0]
+        with torch.cuda.stream(stream):
+            def e2e_step(s):
+                x_in.copy_(xh[s % len(xh)], non_blocking=True)
+                moe.moe_forward(shp, x_in, l0["wr"], l0["bias"], l0["pr"], l0["ps"], rt, ws, y, opts, stream)
+                yh.copy_(y, non_blocking=True)
+            for s in range(3):
+                e2e_step(s)
+            stream.synchronize()
+            Ke = min(K, 2000)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for s in range(Ke):
+                e2e_step(s)
+            b.record(stream)
+            b.synchronize()
+        e_ms = a.elapsed_time(b)
+        res["e2e"] = dict(value=world * T * Ke / (e_ms / 1000.0), unit="routed tokens/s",
+                          h2d_bytes_per_step=T * sh.d * 2, d2h_bytes_per_step=T * sh.d * 2)
+    else:
+        xh = configs.make_decode_x(wl, 16)
+        xh_t = torch.from_numpy(xh.view(np.int16)).pin_memory()
+        yh = torch.empty(1, sh.d, dtype=torch.int16).pin_memory()
+        with torch.cuda.stream(stream):
+            def e2e_step(s):
+                x_in.copy_(xh_t[s % 16:s % 16 + 1], non_blocking=True)
+                graphs["step"].replay()
+                yh.copy_(y, non_blocking=True)
+            for s in range(3):
+                e2e_step(s)
+            stream.synchronize()
+            Ke = min(K, 200)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for s in range(Ke):
+                e2e_step(s)
+            b.record(stream)
+            b.synchronize()
+        e_ms = a.elapsed_time(b)
+        res["e2e"] = dict(value=e_ms * 1000.0 / Ke / layers, unit="us/token/layer",
+                          h2d_bytes_per_step=sh.d * 2, d2h_bytes_per_step=sh.d * 2)
+    return res, wl
+
+
+# ------------------------------------------------------------------------------------- oracle
+def oracle_sample(wl, n_tokens: int, seed: int = 0):
+    """Time the oracle (route + FFN + combine) on a bounded sample of the workload."""
+    import oracle
+    from moe_workload import configs
+    sh = wl.shape
+    lay = configs.make_layer(wl)
+    if sh.T == 1:
+        x = configs.make_decode_x(wl, n_tokens)
+    else:
+        T = wl.chunk or sh.T
+        x_full = configs.make_x(wl)[:T]
+        rng = np.random.default_rng(seed)
+        x = np.ascontiguousarray(x_full[np.sort(rng.choice(T, min(n_tokens, T), replace=False))])
+    t0 = time.perf_counter()
+    r = oracle.route(x, lay.w_router, lay.logit_bias)
+    oracle.moe_tokens(x, r["topk_idx"], r["topk_w"], lay.routed, lay.shared)
+    dt = time.perf_counter() - t0
+    return x.shape[0], dt, oracle.num_threads()
+
+
+def cpu_baseline(wl, n_tokens):
+    n, dt, cores = oracle_sample(wl, n_tokens)
+    if wl.shape.T == 1:
+        return dict(value=dt * 1e6 / n, unit="us/token/layer", cores=cores, kind="oracle",
+                    sample=f"{n} decode tokens through one layer")
+    return dict(value=n / dt, unit="routed tokens/s", cores=cores, kind="oracle",
+                sample=f"{n} of {wl.chunk or wl.shape.T} tokens of one chunk (routing of the sample + FFN + combine)")
+
+
+def run_reference(args, rank, world):
+    from moe_workload import configs
+    wl = configs.WORKLOADS[args.workload]
+    K = args.steps if args.steps is not None else 10
+    n = 4 if wl.shape.T != 1 else 8
+    for s in range(args.warmup):
+        oracle_sample(wl, n, seed=100 + s)
+    tot, toks, cores = 0.0, 0, 1
+    for s in range(K):
+        m, dt, cores = oracle_sample(wl, n, seed=s)
+        tot += dt
+        toks += m
+    decode = wl.shape.T == 1
+    if decode:
+        value, unit, hib = tot * 1e6 / toks, "us/token/layer", False
+    else:
+        value, unit, hib = toks / tot, "routed tokens/s", True
+    sample = f"{n} tokens per step through one layer (routing + FFN + combine)"
+    return dict(impl="reference", metric=METRIC, value=value, unit=unit, n_gpus=world, steps=K, warmup=args.warmup,
+                ms_per_step=tot * 1000.0 / K, higher_is_better=hib, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic",
+                config=dict(workload=wl.name, T=wl.chunk or wl.shape.T, d=wl.shape.d, E=wl.shape.E, k=wl.shape.k,
+                            I=wl.shape.I, I_shared=wl.shape.I_shared, parallelism="host cores"),
+                cpu_baseline=dict(value=value, unit=unit, cores=cores, kind="oracle", sample=sample),
+                e2e=dict(value=value, unit=unit, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)))
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("gloo")
+    res, wl = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_tokens if wl.shape.T != 1 else 16)
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

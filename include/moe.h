@@ -1,0 +1,190 @@
+/* moe.h -- C ABI of the GB300 (sm_103a) sparse-MoE expert path.
+ *
+ * The path (one MoE layer of a hybrid MoE language model; "Optimizing on-device inference
+ * for Apple Silicon", Perplexity Engineering 2026):
+ *   route        router logits over E = 256 experts, top-8, routing weights, per-expert
+ *                histogram, exclusive prefix scan to group offsets, stable scatter of the
+ *                token rows into expert groups, block map of fixed-size row tiles
+ *                (sections "Qwen creates three different workload shapes" and "Keep expert
+ *                routing on the GPU"; tile rows: "Match tile size to expert load").
+ *   grouped_ffn  per expert group: SwiGLU FFN whose 4-bit group-affine weights are rebuilt
+ *                in bf16 tile by tile on chip (64 weights share one bf16 scale and bias,
+ *                w = scale*q + bias), fp32 accumulation; the output projection is weighted by
+ *                the routing score and summed with the always-on shared expert in fp32
+ *                (sections "Dequantize weights during matrix multiplication" and "Reduce
+ *                intermediate and state traffic").
+ *   combine      the fp32 token-order sum is written out as bf16.
+ * Batch-1 decode (T <= options.decode_max_tokens) runs the same calls on GEMV kernels
+ * (section "Optimize the single-row weight path").
+ *
+ * Conventions
+ *   - Every pointer argument named *_dev is CUDA device memory owned by the caller; the
+ *     library never allocates, frees, or keeps pointers between calls.  bf16 values are
+ *     passed as their 16-bit patterns (uint16_t).  All device buffers must be 16-byte
+ *     aligned (256-byte for the workspace).
+ *   - stream is a cudaStream_t passed as void*.  Calls are asynchronous on that stream,
+ *     never synchronise it, and do no device-to-host copies; results are valid when the
+ *     stream reaches them.  The three path calls of one layer must share a stream.
+ *   - Return values: MOE_OK or a negative MOE_ERR_*.  Argument errors are found on the host
+ *     before anything is launched.  Errors found on the device (a routing index out of
+ *     range, a bounded wait that ran out) set bits of the status word kept in the workspace;
+ *     read it with moe_read_status (a synchronising debug call).
+ *   - Supported shapes: E = 256, k = 8, group = 64, d % 256 == 0, I % 128 == 0,
+ *     I_shared == I, d % 128 == 0, 0 <= T <= 65536.  T = 0 is a no-op.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG -1    /* null pointer, negative or inconsistent size, misalignment */
+#define MOE_ERR_UNSUPPORTED -2    /* a shape outside the supported set above */
+#define MOE_ERR_CUDA -3           /* a CUDA runtime call failed (launch, attribute, tensor map) */
+#define MOE_ERR_DEVICE_STATUS -4  /* moe_read_status: the device flagged bad routing data */
+#define MOE_ERR_DEVICE_TIMEOUT -5 /* moe_read_status: a bounded wait inside a kernel ran out */
+#define MOE_ERR_WORKSPACE -6      /* workspace or packed-weight buffer smaller than required */
+
+/* Device status bits (moe_read_status) */
+#define MOE_STATUS_BAD_EXPERT 0x1   /* an expert index outside [0, E) reached the FFN */
+#define MOE_STATUS_TIMEOUT 0x2      /* a pipeline wait gave up */
+
+/* Problem sizes: T tokens, hidden d, E routed experts, top-k, expert intermediate I,
+ * shared-expert intermediate I_shared, quant group (weights per scale/bias). */
+typedef struct moe_shape {
+    int T, d, E, k, I, I_shared, group;
+} moe_shape;
+
+/* One stack of 4-bit group-affine matrices in the checkpoint layout, expert outermost:
+ *   codes  uint8 [n_experts][N][K/2]; code k of a row is the low nibble of byte k/2 for
+ *          even k and the high nibble for odd k; unsigned values 0..15
+ *   scales bf16  [n_experts][N][K/64]   (group g covers weights 64g .. 64g+63 of the row)
+ *   biases bf16  [n_experts][N][K/64]
+ * Weight (n, k) = bf16_round_nearest_even(scale * code + bias) (one rounding). */
+typedef struct moe_q4 {
+    const uint8_t* codes_dev;
+    const uint16_t* scales_dev;
+    const uint16_t* biases_dev;
+} moe_q4;
+
+/* The three projections of num_experts SwiGLU experts.  gate/up: N = I, K = d;
+ * down: N = d, K = I.  h = silu(x.gate) * (x.up); y = h.down. */
+typedef struct moe_expert_weights {
+    moe_q4 gate, up, down;
+    int num_experts;
+} moe_expert_weights;
+
+/* Routing results, all caller-owned device buffers (sizes for T tokens, E experts, top-k):
+ *   topk_idx  int32 [T][k]   expert of slot j (slots in rank order, ties -> lower index)
+ *   topk_w    fp32  [T][k]   routing weights: softmax over the E logits renormalised
+ *                            over the kept k (sum to 1 per token)
+ *   counts    int32 [E]      rows routed to each expert
+ *   offsets   int32 [E+1]    exclusive prefix scan of counts; offsets[E] = k*T
+ *   perm      int32 [k*T]    group row p -> assignment t*k + j (rows of a group ascend in t)
+ *   pos       int32 [T][k]   assignment -> group row (the inverse of perm)
+ *   tiles     int32 [moe_max_tiles(T, tile_rows)][3]  block map (expert, first row, rows),
+ *                            expert-ascending, tile_rows rows each but the last of a group
+ *   num_tiles int32 [1]      number of valid tiles */
+typedef struct moe_routing {
+    int32_t* topk_idx_dev;
+    float* topk_w_dev;
+    int32_t* counts_dev;
+    int32_t* offsets_dev;
+    int32_t* perm_dev;
+    int32_t* pos_dev;
+    int32_t* tiles_dev;
+    int32_t* num_tiles_dev;
+} moe_routing;
+
+/* Options.  Zero-initialise and set what you need; zero fields take the defaults. */
+typedef struct moe_options {
+    int tile_rows;          /* rows per exported block-map tile; default 32 */
+    int decode_max_tokens;  /* T at or below this runs the decode (GEMV) kernels; default 1 */
+    int reserved[6];
+} moe_options;
+
+/* Human-readable text for a return code. */
+const char* moe_error_string(int code);
+
+/* Check a shape against the supported set: MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED. */
+int moe_check_shape(const moe_shape* shape);
+
+/* Bytes of the caller-provided workspace for this shape (0 if the shape is unsupported).
+ * The workspace holds routing scratch, the gathered rows, the intermediate h, the fp32
+ * token-order sum and the device status word.  One workspace serves one stream at a time. */
+size_t moe_workspace_bytes(const moe_shape* shape, const moe_options* options);
+
+/* Number of int32 triples the block map (moe_routing.tiles) can need: ceil(k*T/tile_rows) + E. */
+size_t moe_max_tiles(int T, int k, int E, int tile_rows);
+
+/* Bytes of the device-friendly 4-bit layout of a weight stack (see moe_pack_weights). */
+size_t moe_packed_bytes(const moe_shape* shape, int num_experts, int intermediate);
+
+/* Load-time relayout of one expert-weight stack into the library's packed 4-bit form:
+ * per (expert, 128-row tile, 64-wide K block) one contiguous chunk of codes (nibbles
+ * reordered for register-level unpacking), scales and biases; gate and up chunks are
+ * interleaved.  The packed form is still 4 bits per weight plus the bf16 scale and bias
+ * per group; no bf16 copy of the weights is made.  `intermediate` is I for the routed
+ * stack and I_shared for the shared one.  dst_dev (packed_bytes bytes, caller-owned) is
+ * written asynchronously on stream.  Call once per weight stack, outside any timed region. */
+int moe_pack_weights(const moe_shape* shape, const moe_expert_weights* src, int intermediate, void* dst_dev,
+                     size_t dst_bytes, void* stream);
+
+/* Step a1-a6: router logits (x [T][d] bf16, w_router [E][d] bf16, optional fp32 logit_bias
+ * [E] added after the dot product), top-k with weights, histogram, prefix scan, stable
+ * scatter, block map.  Also gathers the routed rows into expert order inside the workspace
+ * for moe_grouped_ffn and clears the fp32 token-order sum.
+ * The logit of (t, e) is fixed bit-exactly: 32 partial fp32 sums, sum l taking
+ * k = 256*i + 8*l + j (i ascending, j = 0..7) with fused multiply-adds from 0, then the
+ * tree s[i] += s[i+m] for m = 16, 8, 4, 2, 1, then + logit_bias[e]. */
+int moe_route(const moe_shape* shape, const uint16_t* x_dev, const uint16_t* w_router_dev,
+              const float* logit_bias_dev, const moe_routing* routing, void* workspace_dev,
+              size_t workspace_bytes, const moe_options* options, void* stream);
+
+/* Steps a7-a9: for every expert group and the shared expert, gate/up projections with
+ * SwiGLU (h kept to 16 bits as a bf16 pair), output projection, and the fp32 weighted
+ * accumulation into the token-order sum held in the workspace (routing weight topk_w for
+ * routed rows, 1 for the shared expert).  Weights are the packed stacks written by
+ * moe_pack_weights (routed: E experts with I; shared: 1 expert with I_shared).
+ * Requires moe_route on the same workspace and stream first. */
+int moe_grouped_ffn(const moe_shape* shape, const uint16_t* x_dev, const moe_routing* routing,
+                    const void* packed_routed_dev, const void* packed_shared_dev, void* workspace_dev,
+                    size_t workspace_bytes, const moe_options* options, void* stream);
+
+/* Sub-steps of moe_grouped_ffn, in this order (exposed so callers can time them apart):
+ * gate/up + SwiGLU into h, then output projection + weighted accumulation. */
+int moe_ffn_gate_up(const moe_shape* shape, const uint16_t* x_dev, const moe_routing* routing,
+                    const void* packed_routed_dev, const void* packed_shared_dev, void* workspace_dev,
+                    size_t workspace_bytes, const moe_options* options, void* stream);
+int moe_ffn_down(const moe_shape* shape, const moe_routing* routing, const void* packed_routed_dev,
+                 const void* packed_shared_dev, void* workspace_dev, size_t workspace_bytes,
+                 const moe_options* options, void* stream);
+
+/* Step a10: y [T][d] bf16 (round to nearest even) from the fp32 token-order sum. */
+int moe_combine(const moe_shape* shape, const moe_routing* routing, void* workspace_dev, size_t workspace_bytes,
+                uint16_t* y_dev, const moe_options* options, void* stream);
+
+/* The whole layer: moe_route, moe_grouped_ffn, moe_combine in one call. */
+int moe_forward(const moe_shape* shape, const uint16_t* x_dev, const uint16_t* w_router_dev,
+                const float* logit_bias_dev, const void* packed_routed_dev, const void* packed_shared_dev,
+                const moe_routing* routing, void* workspace_dev, size_t workspace_bytes, uint16_t* y_dev,
+                const moe_options* options, void* stream);
+
+/* Synchronise stream, read and clear the device status word of a workspace.
+ * Returns MOE_OK, MOE_ERR_DEVICE_STATUS or MOE_ERR_DEVICE_TIMEOUT; *status_out (if not
+ * null) gets the raw MOE_STATUS_* bits.  A debug/test call: it blocks the host. */
+int moe_read_status(void* workspace_dev, void* stream, int* status_out);
+
+/* Number of kernels this library has launched in this process (diagnostics). */
+unsigned long long moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,317 @@
+// moe_internal.cuh -- shared device/host definitions of the sm_103a MoE path.
+//
+// Inline-PTX wrappers for mbarriers, TMA (cp.async.bulk[.tensor]) and the 5th-generation
+// tensor cores (tcgen05: TMEM allocation, MMA, commit, TMEM loads), the packed 4-bit weight
+// layout, the workspace layout and the bounded-wait machinery.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------------------------
+// Packed 4-bit weight layout (written by moe_pack_weights, read by the FFN kernels).
+//
+// A weight stack [E][N][K] is cut into chunks of 128 rows x 64 input columns (one quant
+// group wide).  Chunk (e, m, kb) holds, contiguously:
+//   codes   4096 B = [2 halves][128 rows][16 B]; half h covers columns 32h..32h+31 of the
+//           K block; 16 B = 4 words, word w covers columns 32h+8w .. +7 with nibble p of the
+//           word (bits 4p..4p+3) holding column offset {0,2,4,6,1,3,5,7}[p], so that
+//           ((word >> 4s) & 0x000F000F) is the consecutive pair (2s, 2s+1) for s = 0..3, each
+//           code sitting in the low mantissa bits of one bf16 half;
+//   scales  256 B = bf16 [128 rows];   biases 256 B = bf16 [128 rows].
+// Gate/up stacks interleave the gate chunk and the up chunk of the same (e, m, kb):
+//   [E][N/128][K/64][2][4608 B].  Down stacks: [E][N/128][K/64][4608 B].
+// ------------------------------------------------------------------------------------
+constexpr int kTileRows = 128;          // rows of a packed chunk = MMA M
+constexpr int kBK = 64;                 // columns of a packed chunk = one quant group
+constexpr int kChunkCodes = 4096;
+constexpr int kChunkBytes = 4608;       // codes + 128 scales + 128 biases
+constexpr int kChunkPairBytes = 2 * kChunkBytes;
+
+// ------------------------------------------------------------------------------------
+// Workspace layout (byte offsets from the caller's workspace pointer, 256-aligned).
+// ------------------------------------------------------------------------------------
+struct WsLayout {
+    size_t status;      // int32[64]: [0] status bits, [1] decode done-counter, [2..] per-tile counters
+    size_t blk;         // int32 [nblk][E] per-block counts, then per-block bases
+    size_t gu_tiles;    // int4 [max_gu]: (expert, row0, rows, mtile)
+    size_t gu_num;      // int32
+    size_t dn_tiles;    // int4 [max_dn]
+    size_t dn_num;      // int32
+    size_t xs;          // bf16 [k*T][d] rows in expert-group order
+    size_t H;           // bf16 [(k+1)*T][2*I] (hi | lo)
+    size_t acc;         // fp32 [T][d] token-order sum
+    size_t dec;         // decode scratch: logits fp32 [8][E], g/u fp32 [8][k+1][2][I]
+    size_t total;
+    int nblk, max_gu, max_dn;
+};
+
+constexpr int kRouteBlockTokens = 32;   // tokens per routing block (one warp, one bitmask)
+constexpr int kMaxN = 256;              // max rows of a GEMM tile (MMA N)
+constexpr int kDecodeMaxT = 8;          // largest T the decode (GEMV) kernels take
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline int gemm_ntile_bound(int rows_total, int groups) {
+    // tiles of <= kMaxN rows, near-equal split per group: at most rows/kMaxN + groups
+    return rows_total / kMaxN + groups + 1;
+}
+
+inline WsLayout ws_layout(const moe_shape& s) {
+    WsLayout L{};
+    const int T = s.T, d = s.d, E = s.E, k = s.k, I = s.I;
+    L.nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
+    const int shared_nt = (T + kMaxN - 1) / kMaxN;
+    const int routed_nt = gemm_ntile_bound(k * T, E);
+    L.max_gu = (routed_nt + shared_nt) * (I / kTileRows);
+    L.max_dn = (routed_nt + shared_nt) * (d / kTileRows);
+    size_t o = 0;
+    L.status = o; o = align_up(o + 64 * 4, 256);
+    L.blk = o; o = align_up(o + (size_t)2 * L.nblk * E * 4, 256);
+    L.gu_tiles = o; o = align_up(o + (size_t)L.max_gu * 16, 256);
+    L.gu_num = o; o = align_up(o + 16, 256);
+    L.dn_tiles = o; o = align_up(o + (size_t)L.max_dn * 16, 256);
+    L.dn_num = o; o = align_up(o + 16, 256);
+    L.xs = o; o = align_up(o + (size_t)k * T * d * 2 + 256 * d * 2, 1024);
+    L.H = o; o = align_up(o + (size_t)(k + 1) * T * 2 * I * 2 + 256 * 2 * I * 2, 1024);
+    L.acc = o; o = align_up(o + (size_t)T * d * 4, 256);
+    L.dec = o; o = align_up(o + (size_t)kDecodeMaxT * E * 4 + (size_t)kDecodeMaxT * (k + 1) * 2 * I * 4, 256);
+    L.total = o;
+    return L;
+}
+
+// ------------------------------------------------------------------------------------
+// Device helpers
+// ------------------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// A wait gives up after this long; the kernel then records MOE_STATUS_TIMEOUT and unwinds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns false when the
+// wait ran out or another role of the CTA already aborted (*abort != 0).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++n & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+// Bulk copy global -> shared (contiguous bytes; 16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 2-D tiled TMA load (coordinates: c0 innermost, in elements).
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------- tcgen05 ------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B
+// apart (SBO), rows of 128 B; start address advanced by 32 B per 16-element K step.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);          // start address  [0,14)
+    d |= (uint64_t)(16u >> 4) << 16;                        // leading byte offset (unused)
+    d |= (uint64_t)(1024u >> 4) << 32;                      // stride byte offset  [32,46)
+    d |= (uint64_t)1 << 46;                                 // descriptor version  [46,48)
+    d |= (uint64_t)2 << 61;                                 // layout: 128B swizzle [61,64)
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major, M x N.
+__device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                       // D format f32
+           | (1u << 7)                     // A format bf16
+           | (1u << 10)                    // B format bf16
+           | ((uint32_t)(N >> 3) << 17)    // N >> 3
+           | ((uint32_t)(M >> 4) << 24);   // M >> 4
+}
+
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on an mbarrier once every tcgen05 operation issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 lanes x 32 bits x 16 columns (one column per register) from TMEM.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------- misc ---------------------------------------------------
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void set_status(int* status, int bits) { atomicOr(status, bits); }
+
+#endif  // __CUDACC__
+
+// ------------------------------------------------------------------------------------
+// Launch wrappers (host), one per translation unit
+// ------------------------------------------------------------------------------------
+struct RouteArgs {
+    int T, d, E, k, tile_rows;
+    const uint16_t* x;
+    const uint16_t* w_router;
+    const float* bias;
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm;
+    int32_t* pos;
+    int32_t* tiles;
+    int32_t* num_tiles;
+    int I;
+    uint8_t* ws;
+    WsLayout L;
+};
+
+struct FfnArgs {
+    int T, d, E, k, I;
+    const uint16_t* x;
+    const int32_t* topk_idx;
+    const float* topk_w;
+    const int32_t* perm;
+    const uint8_t* w_routed;   // packed
+    const uint8_t* w_shared;   // packed
+    uint8_t* ws;
+    WsLayout L;
+    int num_sms;
+};
+
+cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_route_decode(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_down(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_combine(int T, int d, const float* acc, uint16_t* y, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_decode_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_decode_down(const FfnArgs& a, uint16_t* y, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_pack(int E, int N, int K, const moe_q4& m, int pair_slot, int pair_count, uint8_t* dst,
+                        cudaStream_t st, unsigned long long* launches);
+
+// Encodes 2-D bf16 tensor maps (host; driver entry point fetched through the runtime).
+cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                              uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
+
+}  // namespace moe

@@ -1,0 +1,61 @@
+// pack.cu -- load-time relayout of 4-bit weight stacks into the packed chunk format.
+//
+// Input: the checkpoint layout of "Optimizing on-device inference for Apple Silicon"
+// (section "Dequantize weights during matrix multiplication"): 4-bit codes, 64 weights per
+// bf16 scale and bias.  Output: one contiguous 4608-byte chunk per (expert, 128-row tile,
+// 64-column K block) holding codes (nibbles reordered so that a shift and a mask give two
+// consecutive codes in the mantissa of a bf16 pair), then the 128 scales and 128 biases.
+// Still 4 bits per weight: no bf16 copy of the weights is made.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+__global__ void pack_kernel(int E, int N, int K, const uint8_t* __restrict__ codes,
+                            const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases, int slot,
+                            int nslots, uint8_t* __restrict__ dst) {
+    const int MT = N / kTileRows, KB = K / kBK;
+    const size_t total = (size_t)E * MT * KB * kTileRows;
+    const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int r = (int)(idx % kTileRows);
+    size_t rest = idx / kTileRows;
+    const int kb = (int)(rest % KB);
+    rest /= KB;
+    const int mt = (int)(rest % MT);
+    const int e = (int)(rest / MT);
+    const int row = mt * kTileRows + r;
+    const uint8_t* src = codes + ((size_t)e * N + row) * (K / 2) + (size_t)kb * (kBK / 2);
+    uint8_t* chunk = dst + ((((size_t)e * MT + mt) * KB + kb) * nslots + slot) * kChunkBytes;
+    constexpr int kPerm[8] = {0, 2, 4, 6, 1, 3, 5, 7};   // nibble p <- column offset kPerm[p]
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint8_t* sb = src + 16 * h + 4 * w;
+            const uint32_t S = (uint32_t)sb[0] | ((uint32_t)sb[1] << 8) | ((uint32_t)sb[2] << 16) |
+                               ((uint32_t)sb[3] << 24);   // column c at nibble c
+            uint32_t D = 0;
+#pragma unroll
+            for (int p = 0; p < 8; ++p) D |= ((S >> (4 * kPerm[p])) & 0xFu) << (4 * p);
+            *reinterpret_cast<uint32_t*>(chunk + h * 2048 + r * 16 + 4 * w) = D;
+        }
+    const size_t gi = ((size_t)e * N + row) * (K / kBK) + kb;
+    reinterpret_cast<uint16_t*>(chunk + kChunkCodes)[r] = scales[gi];
+    reinterpret_cast<uint16_t*>(chunk + kChunkCodes + 256)[r] = biases[gi];
+}
+
+}  // namespace
+
+cudaError_t launch_pack(int E, int N, int K, const moe_q4& m, int slot, int nslots, uint8_t* dst, cudaStream_t st,
+                        unsigned long long* launches) {
+    const size_t total = (size_t)E * (N / kTileRows) * (K / kBK) * kTileRows;
+    const int threads = 256;
+    const size_t blocks = (total + threads - 1) / threads;
+    pack_kernel<<<(unsigned)blocks, threads, 0, st>>>(E, N, K, m.codes_dev, m.scales_dev, m.biases_dev, slot, nslots,
+                                                       dst);
+    *launches += 1;
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,82 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every declared symbol, and its
+host-side logic (shape checks, sizes, argument validation) answers without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantized_grouped_gemm_gb300 import _lib, build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_path_calls():
+    names = declared_functions()
+    for n in ("moe_route", "moe_grouped_ffn", "moe_combine", "moe_forward", "moe_pack_weights"):
+        assert n in names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+    assert set(names) == set(_lib.exported_symbols())
+
+
+def test_shape_checks(lib):
+    ok = _lib.moe_shape(512, 2048, 256, 8, 512, 512, 64)
+    assert lib.moe_check_shape(ctypes.byref(ok)) == _lib.MOE_OK
+    for bad, rc in [((512, 2048, 128, 8, 512, 512, 64), _lib.MOE_ERR_UNSUPPORTED),
+                    ((512, 2000, 256, 8, 512, 512, 64), _lib.MOE_ERR_UNSUPPORTED),
+                    ((512, 2048, 256, 8, 500, 500, 64), _lib.MOE_ERR_UNSUPPORTED),
+                    ((512, 2048, 256, 8, 512, 256, 64), _lib.MOE_ERR_UNSUPPORTED),
+                    ((512, 2048, 256, 8, 512, 512, 32), _lib.MOE_ERR_UNSUPPORTED),
+                    ((-1, 2048, 256, 8, 512, 512, 64), _lib.MOE_ERR_INVALID_ARG)]:
+        s = _lib.moe_shape(*bad)
+        assert lib.moe_check_shape(ctypes.byref(s)) == rc, bad
+    assert lib.moe_check_shape(None) == _lib.MOE_ERR_INVALID_ARG
+
+
+def test_sizes(lib):
+    s = _lib.moe_shape(4096, 2048, 256, 8, 512, 512, 64)
+    ws = lib.moe_workspace_bytes(ctypes.byref(s), None)
+    # xs (8T x d bf16) + h (9T x 2I bf16) + fp32 sum (T x d) dominate
+    assert ws >= 8 * 4096 * 2048 * 2 + 9 * 4096 * 1024 * 2 + 4096 * 2048 * 4
+    assert ws < 1.1 * (8 * 4096 * 2048 * 2 + 9 * 4096 * 1024 * 2 + 4096 * 2048 * 4) + (1 << 20)
+    # packed bytes = checkpoint bytes: 0.5625 B per weight, 3 matrices of d x I per expert
+    assert lib.moe_packed_bytes(ctypes.byref(s), 256, 512) == 256 * 3 * 2048 * 512 * 9 // 16
+    assert lib.moe_max_tiles(2048, 8, 256, 32) == 16384 // 32 + 256
+    bad = _lib.moe_shape(4096, 2048, 256, 8, 500, 500, 64)
+    assert lib.moe_workspace_bytes(ctypes.byref(bad), None) == 0
+
+
+def test_argument_validation_without_gpu(lib):
+    s = _lib.moe_shape(16, 512, 256, 8, 128, 128, 64)
+    rt = _lib.moe_routing()
+    # null routing/workspace pointers are rejected on the host, before any CUDA call
+    assert lib.moe_route(ctypes.byref(s), None, None, None, ctypes.byref(rt), None, 0, None, None) == \
+        _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_ffn(ctypes.byref(s), None, ctypes.byref(rt), None, None, None, 0, None, None) == \
+        _lib.MOE_ERR_INVALID_ARG
+    opts = _lib.moe_options(32, 4)   # decode kernels take one token
+    assert lib.moe_route(ctypes.byref(s), None, None, None, ctypes.byref(rt), None, 0, ctypes.byref(opts),
+                         None) == _lib.MOE_ERR_UNSUPPORTED
+    # T = 0 is a no-op that returns before looking at any pointer
+    z = _lib.moe_shape(0, 512, 256, 8, 128, 128, 64)
+    assert lib.moe_route(ctypes.byref(z), None, None, None, None, None, 0, None, None) == _lib.MOE_OK
+    assert lib.moe_error_string(_lib.MOE_ERR_WORKSPACE).decode() != "unknown error"
+    assert lib.moe_launch_count() == 0

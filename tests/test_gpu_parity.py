@@ -1,0 +1,167 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Routing (top-k experts, counts, offsets, perm, pos, block map) must match bit-exactly;
+routing weights within 1e-5; the layer output within max |err| <= 2e-2 (|ref| + 1e-2)
+elementwise and relative Frobenius error <= 5e-3 against the oracle's fp64 result.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_grouped_gemm_gb300 as moe
+from moe_workload import configs
+from gpu_helpers import (DeviceLayer, assert_output_close, assert_routing_equal, routing_to_host, run_forward,
+                         to_dev, y_to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(wl, x_rows=None):
+    sh = wl.shape
+    lay = configs.make_layer(wl)
+    x = configs.make_x(wl) if x_rows is None else x_rows
+    T = x.shape[0]
+    shp = moe.shape(T, sh.d, sh.E, sh.k, sh.I, sh.I_shared)
+    return shp, lay, x, DeviceLayer(shp, lay)
+
+
+SMALL = [
+    configs.WORKLOADS["tiny_t128_d512"],
+    configs.custom_workload("ragged_t200_d512_i256", T=200, d=512, I=256),
+    configs.custom_workload("t33_d256_i128", T=33, d=256, I=128),
+    configs.custom_workload("t2_d512_i128", T=2, d=512, I=128),
+    configs.custom_workload("t1_d512_i128", T=1, d=512, I=128),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("split", [False, True], ids=["forward", "three_calls"])
+def test_small_full_parity(wl, split):
+    shp, lay, x, dl = _setup(wl)
+    rt, ws, y = run_forward(shp, dl, to_dev(x), split_calls=split)
+    ref = oracle.route(x, lay.w_router, lay.logit_bias)
+    assert_routing_equal(routing_to_host(rt, shp.T), ref)
+    out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared)
+    assert_output_close(y_to_f64(y)[: shp.T], out_ref, wl.name)
+
+
+FULL = ["prefill_t512_d2048", "prefill_t4096_d2048", "skew_t16384_d2048"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_routing_and_sampled_outputs(name):
+    wl = configs.WORKLOADS[name]
+    x_all = configs.make_x(wl)
+    T = wl.chunk or wl.shape.T
+    shp, lay, _, dl = _setup(wl, x_rows=x_all[:T])
+    chunks = range(0, wl.shape.T, T)
+    for ci, c0 in enumerate(chunks):
+        if ci > 1:       # skewed case: chunks 0 and 1 of 4 (each 4096 tokens)
+            break
+        x = np.ascontiguousarray(x_all[c0:c0 + T])
+        rt, ws, y = run_forward(shp, dl, to_dev(x))
+        ref = oracle.route(x, lay.w_router, lay.logit_bias)
+        assert_routing_equal(routing_to_host(rt, T), ref)
+        rng = np.random.default_rng(ci)
+        toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 14, replace=False)])).astype(np.int32)
+        out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared, toks)
+        assert_output_close(y_to_f64(y)[toks], out_ref, f"{name} chunk {ci}")
+
+
+def test_decode_t1_layer_steps():
+    wl = configs.WORKLOADS["decode_t1_d2048"]
+    sh = wl.shape
+    lay = configs.make_layer(wl)
+    xs = configs.make_decode_x(wl, 3)
+    shp = moe.shape(1, sh.d, sh.E, sh.k, sh.I, sh.I_shared)
+    dl = DeviceLayer(shp, lay)
+    for s in range(3):
+        x = np.ascontiguousarray(xs[s:s + 1])
+        rt, ws, y = run_forward(shp, dl, to_dev(x))
+        ref = oracle.route(x, lay.w_router, lay.logit_bias)
+        assert_routing_equal(routing_to_host(rt, 1), ref)
+        out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared)
+        assert_output_close(y_to_f64(y)[:1], out_ref, f"decode step {s}")
+
+
+def test_decode_path_equals_prefill_path_for_one_token():
+    wl = configs.custom_workload("t1_d1024_i256", T=1, d=1024, I=256)
+    shp, lay, x, dl = _setup(wl)
+    _, _, y_dec = run_forward(shp, dl, to_dev(x), opts=moe.options(decode_max_tokens=1))
+    _, _, y_pre = run_forward(shp, dl, to_dev(x), opts=moe.options(decode_max_tokens=0))
+    ref = oracle.route(x, lay.w_router)
+    out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared)
+    assert_output_close(y_to_f64(y_dec)[:1], out_ref, "decode kernels")
+    assert_output_close(y_to_f64(y_pre)[:1], out_ref, "prefill kernels")
+
+
+def test_concentrated_routing_big_groups():
+    """A logit bias sends every token to experts 0..7: eight groups of T rows (N tiles of
+    256 + remainder), 248 empty experts."""
+    wl = configs.custom_workload("conc_t600_d512_i128", T=600, d=512, I=128)
+    sh = wl.shape
+    lay = configs.make_layer(wl)
+    lay.logit_bias = np.where(np.arange(256) < 8, 50.0, 0.0).astype(np.float32)
+    x = configs.make_x(wl)
+    shp = moe.shape(sh.T, sh.d, sh.E, sh.k, sh.I, sh.I_shared)
+    dl = DeviceLayer(shp, lay)
+    rt, ws, y = run_forward(shp, dl, to_dev(x))
+    ref = oracle.route(x, lay.w_router, lay.logit_bias)
+    assert (ref["counts"][:8] == 600).all() and ref["counts"][8:].sum() == 0
+    assert_routing_equal(routing_to_host(rt, shp.T), ref)
+    toks = np.arange(0, 600, 37, dtype=np.int32)
+    out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared, toks)
+    assert_output_close(y_to_f64(y)[toks], out_ref, "concentrated")
+
+
+def test_tile_rows_option_changes_only_block_map():
+    wl = configs.custom_workload("t70_d256_i128", T=70, d=256, I=128)
+    shp, lay, x, dl = _setup(wl)
+    for bm in (16, 64):
+        opts = moe.options(tile_rows=bm)
+        rt, ws, y = run_forward(shp, dl, to_dev(x), opts=opts)
+        ref = oracle.route(x, lay.w_router, tile_rows=bm)
+        assert_routing_equal(routing_to_host(rt, shp.T), ref)
+
+
+def test_zero_tokens_is_noop():
+    shp = moe.shape(0, 512, I=128)
+    rt = moe.Routing(0)
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(1, 512, dtype=torch.int16, device="cuda")
+    moe.moe_route(shp, x, x, None, rt, ws)          # returns before touching anything
+
+
+def test_repeat_calls_same_workspace_are_stable():
+    wl = configs.custom_workload("t96_d512_i128", T=96, d=512, I=128)
+    shp, lay, x, dl = _setup(wl)
+    rt = moe.Routing(shp.T)
+    ws = moe.workspace(shp)
+    xd = to_dev(x)
+    outs = []
+    for _ in range(3):
+        y = torch.empty(shp.T, shp.d, dtype=torch.int16, device="cuda")
+        moe.moe_forward(shp, xd, dl.w_router, None, dl.packed_routed, dl.packed_shared, rt, ws, y)
+        outs.append(y_to_f64(y))
+    assert moe.moe_read_status(ws)[0] == moe.MOE_OK
+    ref = oracle.route(x, lay.w_router)
+    out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared)
+    for o in outs:
+        assert_output_close(o, out_ref, "repeat")
+
+
+def test_bad_expert_index_sets_status_not_fault():
+    """Corrupt routing (an expert id out of range) fed to the FFN: the kernels flag it in the
+    status word and skip the access."""
+    wl = configs.custom_workload("t1_d512_i128b", T=1, d=512, I=128)
+    shp, lay, x, dl = _setup(wl)
+    rt = moe.Routing(1)
+    ws = moe.workspace(shp)
+    xd = to_dev(x)
+    moe.moe_route(shp, xd, dl.w_router, None, rt, ws)
+    rt.topk_idx[0, 3] = 999
+    moe.moe_grouped_ffn(shp, xd, rt, dl.packed_routed, dl.packed_shared, ws)
+    rc, bits = moe.moe_read_status(ws)
+    assert rc == moe.MOE_ERR_DEVICE_STATUS and bits & moe.MOE_STATUS_BAD_EXPERT
+    assert moe.moe_read_status(ws)[0] == moe.MOE_OK      # cleared
