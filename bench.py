@@ -171,7 +171,7 @@ def run_ours(args, rank, world, local):
     rt = moe.Routing(T)
     ws = moe.workspace(shp)
     y = torch.empty(T, sh.d, dtype=torch.int16, device=dev)
-    x_in = torch.empty(T, sh.d, dtype=torch.int16, device=dev)
+    x_in = torch.zeros(T, sh.d, dtype=torch.int16, device=dev)
     stream = torch.cuda.Stream(device=dev)
     opts = moe.options()
 
@@ -284,7 +284,7 @@ def run_ours(args, rank, world, local):
     if decode:
         us_tok_layer = ms_step * 1000.0 / layers
         res.update(value=us_tok_layer, unit="us/token/layer", higher_is_better=False)
-        bytes_layer = (sh.E * sh.d * 2) + 9 * 3 * (sh.d * sh.I // 2 + sh.d * (sh.I // 64) * 4 * (1 if True else 1))
+        # router weight (bf16) + gate, up, down of 8 routed + 1 shared expert (4-bit + bf16 scale/bias per 64)
         bytes_layer = sh.E * sh.d * 2 + 9 * (3 * sh.d * sh.I // 2 + 3 * sh.d * sh.I // 64 * 4)
         gbs = bytes_layer / (us_tok_layer * 1e-6) / 1e9
         res["roofline"] = dict(bound="hbm", achieved=gbs, peak=P["hbm_gbs"], unit="GB/s", frac=gbs / P["hbm_gbs"],
@@ -370,28 +370,30 @@ def run_ours(args, rank, world, local):
 
 
 # ------------------------------------------------------------------------------------- oracle
-def oracle_sample(wl, n_tokens: int, seed: int = 0):
-    """Time the oracle (route + FFN + combine) on a bounded sample of the workload."""
-    import oracle
-    from moe_workload import configs
-    sh = wl.shape
-    lay = configs.make_layer(wl)
-    if sh.T == 1:
-        x = configs.make_decode_x(wl, n_tokens)
-    else:
-        T = wl.chunk or sh.T
-        x_full = configs.make_x(wl)[:T]
+class OracleSampler:
+    """Times the oracle (route + FFN + combine) on bounded token samples of a workload."""
+
+    def __init__(self, wl):
+        from moe_workload import configs
+        self.wl = wl
+        self.lay = configs.make_layer(wl)
+        sh = wl.shape
+        self.x_pool = configs.make_decode_x(wl, 64) if sh.T == 1 else configs.make_x(wl)[: (wl.chunk or sh.T)]
+
+    def run(self, n_tokens: int, seed: int = 0):
+        import oracle
         rng = np.random.default_rng(seed)
-        x = np.ascontiguousarray(x_full[np.sort(rng.choice(T, min(n_tokens, T), replace=False))])
-    t0 = time.perf_counter()
-    r = oracle.route(x, lay.w_router, lay.logit_bias)
-    oracle.moe_tokens(x, r["topk_idx"], r["topk_w"], lay.routed, lay.shared)
-    dt = time.perf_counter() - t0
-    return x.shape[0], dt, oracle.num_threads()
+        pool = self.x_pool
+        x = np.ascontiguousarray(pool[np.sort(rng.choice(pool.shape[0], min(n_tokens, pool.shape[0]), replace=False))])
+        t0 = time.perf_counter()
+        r = oracle.route(x, self.lay.w_router, self.lay.logit_bias)
+        oracle.moe_tokens(x, r["topk_idx"], r["topk_w"], self.lay.routed, self.lay.shared)
+        dt = time.perf_counter() - t0
+        return x.shape[0], dt, oracle.num_threads()
 
 
 def cpu_baseline(wl, n_tokens):
-    n, dt, cores = oracle_sample(wl, n_tokens)
+    n, dt, cores = OracleSampler(wl).run(n_tokens)
     if wl.shape.T == 1:
         return dict(value=dt * 1e6 / n, unit="us/token/layer", cores=cores, kind="oracle",
                     sample=f"{n} decode tokens through one layer")
@@ -404,11 +406,12 @@ def run_reference(args, rank, world):
     wl = configs.WORKLOADS[args.workload]
     K = args.steps if args.steps is not None else 10
     n = 4 if wl.shape.T != 1 else 8
+    smp = OracleSampler(wl)
     for s in range(args.warmup):
-        oracle_sample(wl, n, seed=100 + s)
+        smp.run(n, seed=100 + s)
     tot, toks, cores = 0.0, 0, 1
     for s in range(K):
-        m, dt, cores = oracle_sample(wl, n, seed=s)
+        m, dt, cores = smp.run(n, seed=s)
         tot += dt
         toks += m
     decode = wl.shape.T == 1

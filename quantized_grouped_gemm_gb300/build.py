@@ -39,7 +39,22 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(d) > os.path.getmtime(obj) for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, defines=(), out: str = None,
+          build_dir: str = None) -> str:
+    """Compile and link; `defines` (e.g. ["MOE_PF_RAW=8"]) override tuning constants, `out` and
+    `build_dir` place a variant library elsewhere."""
+    global BUILD, LIB
+    saved = (BUILD, LIB)
+    if out is not None:
+        LIB, BUILD = out, build_dir or (out + ".objs")
+        force = True
+    try:
+        return _build(force, verbose, ptxas_info, [f"-D{d}" for d in defines])
+    finally:
+        BUILD, LIB = saved
+
+
+def _build(force, verbose, ptxas_info, dflags):
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     jobs = []
@@ -47,7 +62,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         s = os.path.join(CSRC, src)
         o = os.path.join(BUILD, src.replace(".cu", ".o"))
         if force or _stale(o, s) or ptxas_info:
-            extra = ["-Xptxas", "-v"] if ptxas_info else []
+            extra = (["-Xptxas", "-v"] if ptxas_info else []) + dflags
             jobs.append((src, [cc, *_flags(extra), "-c", s, "-o", o]))
 
     def run(job):

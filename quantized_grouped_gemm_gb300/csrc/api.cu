@@ -186,7 +186,7 @@ int moe_pack_weights(const moe_shape* s, const moe_expert_weights* src, int I, v
     unsigned long long n = 0;
     cudaError_t e = launch_pack(E, I, s->d, src->gate, 0, 2, d8, st, &n);
     if (e == cudaSuccess) e = launch_pack(E, I, s->d, src->up, 1, 2, d8, st, &n);
-    if (e == cudaSuccess) e = launch_pack(E, s->d, I, src->down, 0, 1, d8 + (size_t)E * gate_up_bytes(*s, I), st, &n);
+    if (e == cudaSuccess) e = launch_pack(E, s->d, I, src->down, -1, 2, d8 + (size_t)E * gate_up_bytes(*s, I), st, &n);
     g_launches += n;
     return cuda_status(e);
 }

@@ -107,9 +107,11 @@ __global__ void __launch_bounds__(256) decode_down(DecParams p) {
         if (e < 0 || e >= p.E) e = -1;
     }
     const uint8_t* base = nullptr;
+    // down stacks pair the two 128-row halves of each 256-row tile: chunk (mt, kb) sits at
+    // ((mt / 2) * KB + kb) * 9216 + (mt % 2) * 4608
     if (e >= 0)
-        base = s < p.k ? p.w_dn_routed + (size_t)(e * MT + mt) * KB * kChunkBytes
-                       : p.w_dn_shared + (size_t)mt * KB * kChunkBytes;
+        base = (s < p.k ? p.w_dn_routed + (size_t)(e * (MT / 2)) * KB * kChunkPairBytes : p.w_dn_shared) +
+               (size_t)(mt / 2) * KB * kChunkPairBytes + (mt % 2) * kChunkBytes;
     const int hf = threadIdx.x >> 7, r = threadIdx.x & 127;
     const int kb0 = hf * (KB / 2), nkb = KB / 2;
     float acc = 0.f;
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(256) decode_down(DecParams p) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 if (u < nq) {
-                    const uint8_t* ch = base + (size_t)(kb0 + q + u) * kChunkBytes;
+                    const uint8_t* ch = base + (size_t)(kb0 + q + u) * kChunkPairBytes;
                     c[u][0] = ld_nc_v4(ch + r * 16);
                     c[u][1] = ld_nc_v4(ch + 2048 + r * 16);
                     sb[u][0] = __ldg(reinterpret_cast<const uint16_t*>(ch + kChunkCodes) + r);

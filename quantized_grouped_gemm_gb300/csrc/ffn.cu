@@ -7,78 +7,114 @@
 // intermediate and state traffic": gate/up projections fused with the gated activation; the
 // output projection fused with the routing score and the shared-expert result.
 //
-// GB300 design (one persistent CTA per SM, 18 warps):
-//   warps 0-7   dequant: packed chunk (smem) -> bf16 A tile in the 128-byte-swizzled K-major
-//               layout the tensor core reads (w = fma.rn.bf16x2(q, scale, bias): one rounding)
-//   warps 8-15  epilogue: TMEM -> registers -> h (gate/up) or weighted fp32 adds (down)
-//   warp 16     producer: cp.async.bulk of packed weight chunks, TMA tiles of activations
-//   warp 17     MMA issuer (one thread) + TMEM owner
-// Swap-AB: the weights are the M = 128 operand, the expert's token rows are N (16..256, in
-// steps of 16, so small experts waste little), K steps of 64 = one quant group.
+// GB300 design: one persistent CTA per SM; a tile is (expert, block of <= 128 token rows,
+// 256-row weight tile).  Each tcgen05.mma is M = 128 token rows x N = 256 weight rows x K = 16:
+//   gate/up  N = 128 gate rows + the same 128 up rows, so one accumulator row holds g and u of
+//            the token for 128 values of i;
+//   down     N = 256 rows of d; K runs over the hi half of h, then its lo half (h is carried to
+//            16 bits as a bf16 pair).
+// Warp roles (22 warps):
+//   warps 0-15  dequant: packed chunk pair (smem) -> bf16 B tile (256 rows x 64) in the 128-byte
+//               swizzled K-major layout the tensor core reads; w = fma.rn.bf16x2(q, scale, bias)
+//   warps 16-19 epilogue: TMEM -> registers; one token row per thread
+//   warp 20     producer: cp.async.bulk of 9216-byte weight pairs, TMA tiles of activations
+//   warp 21     MMA issuer (one thread) and TMEM owner (2 accumulators of 256 columns)
 // All waits are bounded (MOE_STATUS_TIMEOUT, then the CTA unwinds).
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kDeqWarps = 8;
-constexpr int kEpiWarps = 8;
-constexpr int kProdWarp = kDeqWarps + kEpiWarps;   // 16
-constexpr int kMmaWarp = kProdWarp + 1;            // 17
-constexpr int kThreads = (kMmaWarp + 1) * 32;      // 576
+constexpr int kDeqWarps = 16;
+constexpr int kEpiWarps = 4;
+constexpr int kProdWarp = kDeqWarps + kEpiWarps;   // 20
+constexpr int kMmaWarp = kProdWarp + 1;            // 21
+constexpr int kThreads = (kMmaWarp + 1) * 32;      // 704
 
-constexpr int kBStageBytes = kMaxN * 128;          // 256 rows x 64 bf16
-constexpr int kBoxRows = 64;
-constexpr int kBoxBytes = kBoxRows * 128;
-constexpr int kATileBytes = kTileRows * 128;       // 128 rows x 64 bf16
+constexpr int kTokRows = 128;                      // MMA M: token rows of a tile
+constexpr int kWRows = 256;                        // MMA N: weight rows of a tile
+constexpr int kActBytes = kTokRows * 128;          // 128 rows x 64 bf16 (one K block)
+constexpr int kWdqBytes = kWRows * 128;            // 256 rows x 64 bf16
+constexpr int kRawBytes = kChunkPairBytes;         // 9216
 
-// gate/up ring depths
-constexpr int kGuRaw = 6, kGuB = 3, kGuA = 2;
-// down ring depths (B carries the hi and the lo half of h as separate K steps)
-constexpr int kDnRaw = 6, kDnB = 4, kDnA = 2;
+#ifndef MOE_GU_RAW
+#define MOE_GU_RAW 8
+#endif
+#ifndef MOE_GU_WDQ
+#define MOE_GU_WDQ 3
+#endif
+#ifndef MOE_GU_ACT
+#define MOE_GU_ACT 3
+#endif
+#ifndef MOE_DN_RAW
+#define MOE_DN_RAW 6
+#endif
+#ifndef MOE_DN_WDQ
+#define MOE_DN_WDQ 3
+#endif
+#ifndef MOE_DN_ACT
+#define MOE_DN_ACT 4
+#endif
+template <bool kDown>
+struct Cfg {
+    static constexpr int RAW = kDown ? MOE_DN_RAW : MOE_GU_RAW;   // weight-pair ring (HBM -> smem)
+    static constexpr int WDQ = kDown ? MOE_DN_WDQ : MOE_GU_WDQ;   // dequantised weight ring
+    static constexpr int ACT = kDown ? MOE_DN_ACT : MOE_GU_ACT;   // activation ring (TMA)
+    static constexpr int PARTS = kDown ? 2 : 1;    // activation K steps per weight K block
+    static constexpr int act_off = 0;
+    static constexpr int wdq_off = act_off + ACT * kActBytes;
+    static constexpr int raw_off = wdq_off + WDQ * kWdqBytes;
+    static constexpr int bar_off = raw_off + RAW * kRawBytes;
+};
 
 struct Bars {
-    uint64_t raw_full[8], raw_empty[8], b_full[8], b_empty[8], a_full[4], a_empty[4];
+    uint64_t raw_full[8], raw_empty[8], act_full[8], act_empty[8], wdq_full[4], wdq_empty[4];
     uint64_t tm_full[2], tm_empty[2], drain;
     uint32_t tmem_slot;
     int abort;
 };
 
-template <int RAW, int BST, int AST, int ABYTES, int RAWBYTES>
-struct SmemPlan {
-    static constexpr int b_off = 0;
-    static constexpr int a_off = b_off + BST * kBStageBytes;
-    static constexpr int raw_off = a_off + AST * ABYTES;
-    static constexpr int bar_off = raw_off + RAW * RAWBYTES;
-    static constexpr int bytes = bar_off + (int)sizeof(Bars) + 1024;   // + alignment slack
-};
-using GuPlan = SmemPlan<kGuRaw, kGuB, kGuA, 2 * kATileBytes, kChunkPairBytes>;
-using DnPlan = SmemPlan<kDnRaw, kDnB, kDnA, kATileBytes, kChunkBytes>;
-static_assert(GuPlan::bytes <= 232448, "gate/up smem");
-static_assert(DnPlan::bytes <= 232448, "down smem");
+template <bool kDown>
+constexpr int smem_bytes() {
+    return Cfg<kDown>::bar_off + (int)sizeof(Bars) + 1024;   // + alignment slack
+}
+static_assert(smem_bytes<false>() <= 232448, "gate/up smem");
+static_assert(smem_bytes<true>() <= 232448, "down smem");
+
+// Weight chunks come from HBM and run up to RAW K blocks ahead of the activation tiles.
+// No deadlock: a wait on raw_empty for K block g needs the MMA of K block g - RAW - WDQ,
+// whose activation tiles were issued earlier.
+
+#ifdef MOE_TRACE
+constexpr int kTraceK = 96;
+#define TRACE(ev, g)                                                                     \
+    do {                                                                                 \
+        if (blockIdx.x == 0 && (g) < kTraceK) p.trace[(ev) * kTraceK + (g)] = clock64(); \
+    } while (0)
+#else
+#define TRACE(ev, g) \
+    do {             \
+    } while (0)
+#endif
+enum { TR_PRAW = 0, TR_PACT, TR_DWAIT, TR_DDONE, TR_MWAIT, TR_MDONE, TR_ETILE, TR_EDONE, TR_N };
 
 struct FfnParams {
-    const uint8_t* w_routed;   // packed stack (gate/up interleaved, or down)
+    const uint8_t* w_routed;   // packed stack: [E][tiles][K/64][2][4608]
     const uint8_t* w_shared;
-    const int4* tiles;         // (expert, first row, rows, M tile); expert == E: shared
+    const int4* tiles;         // (expert, first row, rows, weight tile); expert == E: shared
     const int* num_tiles;
     uint16_t* H;               // [(k+1)T][2I] bf16, hi | lo
     float* acc;                // [T][d] fp32 token-order sum
     const int32_t* perm;
     const float* topk_w;
     int* status;
+    unsigned long long* trace;
     int T, d, I, E, k;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     const uint32_t s = smem_u32(p);
     return p + ((1024u - (s & 1023u)) & 1023u);
-}
-
-// every lane waits; the outcome is made warp-uniform
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    const bool ok = mbar_wait(bar, parity, abort);
-    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* abort, int* status) {
@@ -94,10 +130,7 @@ __device__ void drain_ring(uint64_t* full, int depth, uint32_t issued) {
     for (uint32_t i = first; i < issued; ++i) mbar_wait(&full[i % depth], (i / depth) & 1, &never);
 }
 
-__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
-
-// Walks this CTA's (tile, K block, part) sequence; part counts the B steps of one K block
-// (1 for gate/up; 2 for down: the hi and the lo half of h).
+// Walks this CTA's (tile, K block, part) sequence.
 struct Cursor {
     int tile, kb, part, num, KB, parts;
     int4 t;
@@ -118,25 +151,7 @@ struct Cursor {
     }
 };
 
-// Weight chunks come from HBM and run up to kLead K blocks ahead of the activation tiles
-// (from L2).  No deadlock: a wait on raw_empty for K step g needs the MMA of step
-// g - RAW - AST, whose activation tile is already issued because kLead < RAW + AST.
-constexpr int kLead = 5;
-
-
-// Which TMEM buffers (256 columns each) a tile uses: N <= 128 -> one (alternating);
-// N > 128 -> both.  Producer-side and consumer-side iterate identically.
-struct TmemSched {
-    int next = 0;
-    uint32_t use[2] = {0, 0};
-    __device__ __forceinline__ int pick(int N, int (&bufs)[2]) {
-        if (N <= 128) { bufs[0] = next; next ^= 1; return 1; }
-        bufs[0] = 0; bufs[1] = 1; return 2;
-    }
-};
-
-// -------- dequant of one packed 128-row half-chunk into the swizzled A layout ---------
-// w (16 B of codes, 32 weights) -> 4 output chunks of 8 bf16 at chunk index c0..c0+3.
+// -------- dequant of 32 weights (one half row of a packed chunk) into the swizzled layout ----
 __device__ __forceinline__ void dequant_store4(uint4 codes, uint32_t s2, uint32_t b2, uint8_t* row_dst, int r,
                                                int c0) {
     const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
@@ -164,227 +179,42 @@ __device__ __forceinline__ void dequant_store4(uint4 codes, uint32_t s2, uint32_
     }
 }
 
-// ======================================================================================
-// gate/up + SwiGLU
-// ======================================================================================
-__global__ void __launch_bounds__(kThreads, 1)
-    ffn_gate_up_kernel(const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_x,
-                       FfnParams p) {
-    extern __shared__ uint8_t smem_dyn[];
-    const int num = *p.num_tiles;
-    if ((int)blockIdx.x >= num) return;
-    uint8_t* smem = align1024(smem_dyn);
-    uint8_t* bstage = smem + GuPlan::b_off;
-    uint8_t* astage = smem + GuPlan::a_off;
-    uint8_t* raw = smem + GuPlan::raw_off;
-    Bars* bars = reinterpret_cast<Bars*>(smem + GuPlan::bar_off);
-    volatile int* abort = &bars->abort;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int KB = p.d / kBK, MT = p.I / kTileRows;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kGuRaw; ++i) { mbar_init(&bars->raw_full[i], 1); mbar_init(&bars->raw_empty[i], kDeqWarps); }
-        for (int i = 0; i < kGuB; ++i) { mbar_init(&bars->b_full[i], 1); mbar_init(&bars->b_empty[i], 1); }
-        for (int i = 0; i < kGuA; ++i) { mbar_init(&bars->a_full[i], kDeqWarps); mbar_init(&bars->a_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&bars->tm_full[i], 1); mbar_init(&bars->tm_empty[i], kEpiWarps); }
-        mbar_init(&bars->drain, 1);
-        bars->abort = 0;
-        fence_barrier_init();
-    }
-    if (warp == kProdWarp && lane == 0) { prefetch_tmap(&tm_xs); prefetch_tmap(&tm_x); }
-    if (warp == kMmaWarp) { tmem_alloc(&bars->tmem_slot, 512); tmem_relinquish(); }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = bars->tmem_slot;
-
-    if (warp == kProdWarp) {
-        if (lane == 0) {
-            uint32_t rit = 0, bit = 0;
-            bool ok = true;
-            Cursor cr, cb;
-            cr.init(p.tiles, num, KB, 1);
-            cb.init(p.tiles, num, KB, 1);
-            while (ok && !cb.done()) {
-                while (ok && !cr.done() && rit < bit + kLead + 1) {
-                    const int e = cr.t.x, mt = cr.t.w;
-                    const uint8_t* wsrc = e < p.E ? p.w_routed + (size_t)(e * MT + mt) * KB * kChunkPairBytes
-                                                  : p.w_shared + (size_t)mt * KB * kChunkPairBytes;
-                    const int rs = rit % kGuRaw;
-                    if (!mbar_wait(&bars->raw_empty[rs], ((rit / kGuRaw) & 1) ^ 1, abort)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&bars->raw_full[rs], kChunkPairBytes);
-                    bulk_g2s(raw + rs * kChunkPairBytes, wsrc + (size_t)cr.kb * kChunkPairBytes, kChunkPairBytes,
-                             &bars->raw_full[rs]);
-                    ++rit;
-                    cr.next();
-                }
-                if (!ok) break;
-                const int e = cb.t.x, row0 = cb.t.y, N = round16(cb.t.z);
-                const int nbox = (N + kBoxRows - 1) / kBoxRows;
-                const CUtensorMap* tm = e < p.E ? &tm_xs : &tm_x;
-                const int bs = bit % kGuB;
-                if (!mbar_wait(&bars->b_empty[bs], ((bit / kGuB) & 1) ^ 1, abort)) { ok = false; break; }
-                mbar_arrive_expect_tx(&bars->b_full[bs], nbox * kBoxBytes);
-                for (int bx = 0; bx < nbox; ++bx)
-                    tma_load_2d(bstage + bs * kBStageBytes + bx * kBoxBytes, tm, cb.kb * kBK, row0 + bx * kBoxRows,
-                                &bars->b_full[bs]);
-                ++bit;
-                cb.next();
-            }
-            if (!ok) raise_abort(abort, p.status);
-            drain_ring(bars->raw_full, kGuRaw, rit);
-            drain_ring(bars->b_full, kGuB, bit);
-        }
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) {
-            uint32_t ait = 0, bit = 0;
-            TmemSched ts;
-            bool ok = true;
-            const uint32_t a_base = smem_u32(astage), b_base = smem_u32(bstage);
-            for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
-                const int4 t = p.tiles[tile];
-                const int N = round16(t.z);
-                int bufs[2];
-                const int nb = ts.pick(N, bufs);
-                for (int q = 0; q < nb; ++q)
-                    if (!mbar_wait(&bars->tm_empty[bufs[q]], (ts.use[bufs[q]] & 1) ^ 1, abort)) ok = false;
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t gate_col = nb == 1 ? 256u * bufs[0] : 0u;
-                const uint32_t up_col = nb == 1 ? gate_col + 128u : 256u;
-                const uint32_t idesc = idesc_bf16_f32(128, N);
-                for (int kb = 0; kb < KB; ++kb) {
-                    const int as = ait % kGuA, bs = bit % kGuB;
-                    if (!mbar_wait(&bars->a_full[as], (ait / kGuA) & 1, abort)) { ok = false; break; }
-                    if (!mbar_wait(&bars->b_full[bs], (bit / kGuB) & 1, abort)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint32_t aoff = a_base + as * 2 * kATileBytes + ks * 32;
-                        const uint64_t bd = sw128_desc(b_base + bs * kBStageBytes + ks * 32);
-                        const uint32_t accum = (kb | ks) ? 1u : 0u;
-                        tc_mma_bf16(tmem + gate_col, sw128_desc(aoff), bd, idesc, accum);
-                        tc_mma_bf16(tmem + up_col, sw128_desc(aoff + kATileBytes), bd, idesc, accum);
-                    }
-                    tc_commit(&bars->a_empty[as]);
-                    tc_commit(&bars->b_empty[bs]);
-                    ++ait;
-                    ++bit;
-                }
-                if (!ok) break;
-                for (int q = 0; q < nb; ++q) { tc_commit(&bars->tm_full[bufs[q]]); ts.use[bufs[q]]++; }
-            }
-            if (!ok) raise_abort(abort, p.status);
-            tc_commit(&bars->drain);
-            int never = 0;
-            mbar_wait(&bars->drain, 0, &never);
-        }
-    } else if (warp < kDeqWarps) {
-        // dequant: thread -> (matrix: 0 gate / 1 up, row r); 64 weights per K block
-        const int mat = threadIdx.x >> 7, r = threadIdx.x & 127;
-        uint32_t rit = 0, ait = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
-            for (int kb = 0; kb < KB; ++kb) {
-                const int rs = rit % kGuRaw, as = ait % kGuA;
-                if (!warp_wait(&bars->raw_full[rs], (rit / kGuRaw) & 1, abort) ||
-                    !warp_wait(&bars->a_empty[as], ((ait / kGuA) & 1) ^ 1, abort)) { ok = false; break; }
-                const uint8_t* ch = raw + rs * kChunkPairBytes + mat * kChunkBytes;
-                const uint4 c0 = *reinterpret_cast<const uint4*>(ch + r * 16);
-                const uint4 c1 = *reinterpret_cast<const uint4*>(ch + 2048 + r * 16);
-                const uint32_t s = *reinterpret_cast<const uint16_t*>(ch + kChunkCodes + 2 * r);
-                const uint32_t b = *reinterpret_cast<const uint16_t*>(ch + kChunkCodes + 256 + 2 * r);
-                uint8_t* row_dst = astage + as * 2 * kATileBytes + mat * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
-                dequant_store4(c0, s * 0x10001u, b * 0x10001u, row_dst, r, 0);
-                dequant_store4(c1, s * 0x10001u, b * 0x10001u, row_dst, r, 4);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) { mbar_arrive(&bars->raw_empty[rs]); mbar_arrive(&bars->a_full[as]); }
-                ++rit;
-                ++ait;
-            }
-        }
-        if (!ok && lane == 0) raise_abort(abort, p.status);
-    } else {
-        // epilogue: h = silu(g) * u, stored as the bf16 pair (hi, lo = h - hi)
-        const int q = warp & 3, g = (warp - kDeqWarps) >> 2;
-        TmemSched ts;
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
-            const int4 t = p.tiles[tile];
-            const int e = t.x, row0 = t.y, rows = t.z, N = round16(t.z), mt = t.w;
-            int bufs[2];
-            const int nb = ts.pick(N, bufs);
-            for (int qq = 0; qq < nb; ++qq)
-                if (!warp_wait(&bars->tm_full[bufs[qq]], ts.use[bufs[qq]] & 1, abort)) ok = false;
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t gate_col = nb == 1 ? 256u * bufs[0] : 0u;
-            const uint32_t up_col = nb == 1 ? gate_col + 128u : 256u;
-            const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-            const int i = mt * kTileRows + 32 * q + lane;
-            const size_t hrow0 = e < p.E ? (size_t)row0 : (size_t)p.k * p.T + row0;
-            uint16_t* Hp = p.H + hrow0 * 2 * p.I + i;
-            for (int c = g; c < N / 16; c += 2) {
-                uint32_t G[16], U[16];
-                tmem_ld16(tmem + lane_base + gate_col + 16 * c, G);
-                tmem_ld16(tmem + lane_base + up_col + 16 * c, U);
-                tmem_ld_wait();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int j = 16 * c + jj;
-                    if (j < rows) {
-                        const float gv = __uint_as_float(G[jj]), uv = __uint_as_float(U[jj]);
-                        const float h = gv / (1.0f + __expf(-gv)) * uv;
-                        const uint16_t hi = f32_to_bf16_rn(h);
-                        const uint16_t lo = f32_to_bf16_rn(h - bf16f(hi));
-                        Hp[(size_t)j * 2 * p.I] = hi;
-                        Hp[(size_t)j * 2 * p.I + p.I] = lo;
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                for (int qq = 0; qq < nb; ++qq) mbar_arrive(&bars->tm_empty[bufs[qq]]);
-            for (int qq = 0; qq < nb; ++qq) ts.use[bufs[qq]]++;
-        }
-        if (!ok && lane == 0) raise_abort(abort, p.status);
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    return (uint32_t)f32_to_bf16_rn(a) | ((uint32_t)f32_to_bf16_rn(b) << 16);
 }
 
 // ======================================================================================
-// down projection + weighted fp32 accumulation into the token-order sum
+// The kernel: kDown == false -> gate/up + SwiGLU into h; true -> down + weighted fp32 sums.
+// tm_a: activations of routed rows (xs for gate/up, h for down); tm_b: the shared expert's
+// activation rows (x for gate/up; unused for down, whose shared rows follow in h).
 // ======================================================================================
+template <bool kDown>
 __global__ void __launch_bounds__(kThreads, 1)
-    ffn_down_kernel(const __grid_constant__ CUtensorMap tm_h, FfnParams p) {
+    ffn_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, FfnParams p) {
+    using C = Cfg<kDown>;
     extern __shared__ uint8_t smem_dyn[];
     const int num = *p.num_tiles;
     if ((int)blockIdx.x >= num) return;
     uint8_t* smem = align1024(smem_dyn);
-    uint8_t* bstage = smem + DnPlan::b_off;
-    uint8_t* astage = smem + DnPlan::a_off;
-    uint8_t* raw = smem + DnPlan::raw_off;
-    Bars* bars = reinterpret_cast<Bars*>(smem + DnPlan::bar_off);
+    uint8_t* act = smem + C::act_off;
+    uint8_t* wdq = smem + C::wdq_off;
+    uint8_t* raw = smem + C::raw_off;
+    Bars* bars = reinterpret_cast<Bars*>(smem + C::bar_off);
     volatile int* abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int KB = p.I / kBK, MT = p.d / kTileRows;
+    const int KB = (kDown ? p.I : p.d) / kBK;                  // weight K blocks
+    const int WT = (kDown ? p.d : p.I * 2) / kWRows;          // weight tiles per expert
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kDnRaw; ++i) { mbar_init(&bars->raw_full[i], 1); mbar_init(&bars->raw_empty[i], kDeqWarps); }
-        for (int i = 0; i < kDnB; ++i) { mbar_init(&bars->b_full[i], 1); mbar_init(&bars->b_empty[i], 1); }
-        for (int i = 0; i < kDnA; ++i) { mbar_init(&bars->a_full[i], kDeqWarps); mbar_init(&bars->a_empty[i], 1); }
+        for (int i = 0; i < C::RAW; ++i) { mbar_init(&bars->raw_full[i], 1); mbar_init(&bars->raw_empty[i], kDeqWarps); }
+        for (int i = 0; i < C::ACT; ++i) { mbar_init(&bars->act_full[i], 1); mbar_init(&bars->act_empty[i], 1); }
+        for (int i = 0; i < C::WDQ; ++i) { mbar_init(&bars->wdq_full[i], kDeqWarps); mbar_init(&bars->wdq_empty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&bars->tm_full[i], 1); mbar_init(&bars->tm_empty[i], kEpiWarps); }
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_barrier_init();
     }
-    if (warp == kProdWarp && lane == 0) prefetch_tmap(&tm_h);
+    if (warp == kProdWarp && lane == 0) { prefetch_tmap(&tm_a); if (!kDown) prefetch_tmap(&tm_b); }
     if (warp == kMmaWarp) { tmem_alloc(&bars->tmem_slot, 512); tmem_relinquish(); }
     tc_fence_before();
     __syncthreads();
@@ -393,73 +223,76 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kProdWarp) {
         if (lane == 0) {
-            uint32_t rit = 0, bit = 0;
+            uint32_t rit = 0, ait = 0;
             bool ok = true;
-            Cursor cr, cb;
+            Cursor cr, ca;
             cr.init(p.tiles, num, KB, 1);
-            cb.init(p.tiles, num, KB, 2);
-            while (ok && !cb.done()) {
-                while (ok && !cr.done() && rit < bit / 2 + kLead + 1) {
-                    const int e = cr.t.x, mt = cr.t.w;
-                    const uint8_t* wsrc = e < p.E ? p.w_routed + (size_t)(e * MT + mt) * KB * kChunkBytes
-                                                  : p.w_shared + (size_t)mt * KB * kChunkBytes;
-                    const int rs = rit % kDnRaw;
-                    if (!mbar_wait(&bars->raw_empty[rs], ((rit / kDnRaw) & 1) ^ 1, abort)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&bars->raw_full[rs], kChunkBytes);
-                    bulk_g2s(raw + rs * kChunkBytes, wsrc + (size_t)cr.kb * kChunkBytes, kChunkBytes,
-                             &bars->raw_full[rs]);
+            ca.init(p.tiles, num, KB, C::PARTS);
+            while (ok && !ca.done()) {
+                while (ok && !cr.done() && rit < ait / C::PARTS + C::RAW) {
+                    const int e = cr.t.x, wt = cr.t.w;
+                    const uint8_t* w = (e < p.E ? p.w_routed + (size_t)(e * WT + wt) * KB * kRawBytes
+                                                : p.w_shared + (size_t)wt * KB * kRawBytes) +
+                                       (size_t)cr.kb * kRawBytes;
+                    const int rs = rit % C::RAW;
+                    if (!mbar_wait(&bars->raw_empty[rs], ((rit / C::RAW) & 1) ^ 1, abort)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&bars->raw_full[rs], kRawBytes);
+                    bulk_g2s(raw + rs * kRawBytes, w, kRawBytes, &bars->raw_full[rs]);
+                    TRACE(TR_PRAW, rit);
                     ++rit;
                     cr.next();
                 }
                 if (!ok) break;
-                const int e = cb.t.x, row0 = cb.t.y, N = round16(cb.t.z);
-                const int nbox = (N + kBoxRows - 1) / kBoxRows;
-                const int hrow0 = e < p.E ? row0 : p.k * p.T + row0;
-                const int bs = bit % kDnB;
-                if (!mbar_wait(&bars->b_empty[bs], ((bit / kDnB) & 1) ^ 1, abort)) { ok = false; break; }
-                mbar_arrive_expect_tx(&bars->b_full[bs], nbox * kBoxBytes);
-                for (int bx = 0; bx < nbox; ++bx)
-                    tma_load_2d(bstage + bs * kBStageBytes + bx * kBoxBytes, &tm_h, cb.part * p.I + cb.kb * kBK,
-                                hrow0 + bx * kBoxRows, &bars->b_full[bs]);
-                ++bit;
-                cb.next();
+                const int e = ca.t.x, row0 = ca.t.y;
+                const int as = ait % C::ACT;
+                if (!mbar_wait(&bars->act_empty[as], ((ait / C::ACT) & 1) ^ 1, abort)) { ok = false; break; }
+                mbar_arrive_expect_tx(&bars->act_full[as], kActBytes);
+                if (kDown) {
+                    const int hrow0 = e < p.E ? row0 : p.k * p.T + row0;
+                    tma_load_2d(act + as * kActBytes, &tm_a, ca.part * p.I + ca.kb * kBK, hrow0, &bars->act_full[as]);
+                } else {
+                    tma_load_2d(act + as * kActBytes, e < p.E ? &tm_a : &tm_b, ca.kb * kBK, row0, &bars->act_full[as]);
+                }
+                TRACE(TR_PACT, ait);
+                ++ait;
+                ca.next();
             }
             if (!ok) raise_abort(abort, p.status);
-            drain_ring(bars->raw_full, kDnRaw, rit);
-            drain_ring(bars->b_full, kDnB, bit);
+            drain_ring(bars->raw_full, C::RAW, rit);
+            drain_ring(bars->act_full, C::ACT, ait);
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            uint32_t ait = 0, bit = 0, tcount = 0;
+            uint32_t wit = 0, ait = 0, tcount = 0;
             uint32_t use[2] = {0, 0};
             bool ok = true;
-            const uint32_t a_base = smem_u32(astage), b_base = smem_u32(bstage);
+            const uint32_t act_base = smem_u32(act), wdq_base = smem_u32(wdq);
+            const uint32_t idesc = idesc_bf16_f32(kTokRows, kWRows);
             for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x, ++tcount) {
-                const int4 t = p.tiles[tile];
-                const int N = round16(t.z);
                 const int buf = tcount & 1;
                 if (!mbar_wait(&bars->tm_empty[buf], (use[buf] & 1) ^ 1, abort)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t dcol = 256u * buf;
-                const uint32_t idesc = idesc_bf16_f32(128, N);
+                const uint32_t dcol = tmem + 256u * buf;
                 for (int kb = 0; kb < KB && ok; ++kb) {
-                    const int as = ait % kDnA;
-                    if (!mbar_wait(&bars->a_full[as], (ait / kDnA) & 1, abort)) { ok = false; break; }
-                    for (int part = 0; part < 2; ++part) {
-                        const int bs = bit % kDnB;
-                        if (!mbar_wait(&bars->b_full[bs], (bit / kDnB) & 1, abort)) { ok = false; break; }
+                    const int ws = wit % C::WDQ;
+                    if (!mbar_wait(&bars->wdq_full[ws], (wit / C::WDQ) & 1, abort)) { ok = false; break; }
+                    TRACE(TR_MWAIT, wit);
+                    for (int part = 0; part < C::PARTS; ++part) {
+                        const int as = ait % C::ACT;
+                        if (!mbar_wait(&bars->act_full[as], (ait / C::ACT) & 1, abort)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t ad = sw128_desc(a_base + as * kATileBytes + ks * 32);
-                            const uint64_t bd = sw128_desc(b_base + bs * kBStageBytes + ks * 32);
-                            tc_mma_bf16(tmem + dcol, ad, bd, idesc, (kb | part | ks) ? 1u : 0u);
+                            const uint64_t ad = sw128_desc(act_base + as * kActBytes + ks * 32);
+                            const uint64_t bd = sw128_desc(wdq_base + ws * kWdqBytes + ks * 32);
+                            tc_mma_bf16(dcol, ad, bd, idesc, (kb | part | ks) ? 1u : 0u);
                         }
-                        tc_commit(&bars->b_empty[bs]);
-                        ++bit;
+                        tc_commit(&bars->act_empty[as]);
+                        ++ait;
                     }
-                    tc_commit(&bars->a_empty[as]);
-                    ++ait;
+                    tc_commit(&bars->wdq_empty[ws]);
+                    TRACE(TR_MDONE, wit);
+                    ++wit;
                 }
                 if (!ok) break;
                 tc_commit(&bars->tm_full[buf]);
@@ -471,69 +304,118 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bars->drain, 0, &never);
         }
     } else if (warp < kDeqWarps) {
-        // dequant: thread -> (row r, half hf); 32 weights per K block
-        const int hf = threadIdx.x >> 7, r = threadIdx.x & 127;
-        uint32_t rit = 0, ait = 0;
+        // dequant: thread -> (weight row r of the 256-row tile, half hf); 32 weights per K block.
+        // Rows 0..127 come from the first chunk of the pair, rows 128..255 from the second.
+        // Every warp waits on its own (lock-stepping the 16 warps on a named barrier measured
+        // slower: a warp may start the next K block while others finish this one).
+        const int r = threadIdx.x & 255, hf = threadIdx.x >> 8;
+        const int mat = r >> 7, rr = r & 127;
+        const uint32_t code_off = mat * kChunkBytes + hf * 2048 + rr * 16;
+        const uint32_t sb_off = mat * kChunkBytes + kChunkCodes + 2 * rr;
+        const uint32_t row_off = (r >> 3) * 1024 + (r & 7) * 128;
+        uint32_t rit = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
             for (int kb = 0; kb < KB; ++kb) {
-                const int rs = rit % kDnRaw, as = ait % kDnA;
-                if (!warp_wait(&bars->raw_full[rs], (rit / kDnRaw) & 1, abort) ||
-                    !warp_wait(&bars->a_empty[as], ((ait / kDnA) & 1) ^ 1, abort)) { ok = false; break; }
-                const uint8_t* ch = raw + rs * kChunkBytes;
-                const uint4 cw = *reinterpret_cast<const uint4*>(ch + hf * 2048 + r * 16);
-                const uint32_t s = *reinterpret_cast<const uint16_t*>(ch + kChunkCodes + 2 * r);
-                const uint32_t b = *reinterpret_cast<const uint16_t*>(ch + kChunkCodes + 256 + 2 * r);
-                uint8_t* row_dst = astage + as * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
-                dequant_store4(cw, s * 0x10001u, b * 0x10001u, row_dst, r, 4 * hf);
+                const int rs = rit % C::RAW, ws = rit % C::WDQ;
+                const bool got = mbar_wait(&bars->raw_full[rs], (rit / C::RAW) & 1, abort) &&
+                                 mbar_wait(&bars->wdq_empty[ws], ((rit / C::WDQ) & 1) ^ 1, abort);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                if (threadIdx.x == 0) TRACE(TR_DWAIT, rit);
+                const uint8_t* ch = raw + rs * kRawBytes;
+                const uint4 cw = *reinterpret_cast<const uint4*>(ch + code_off);
+                const uint32_t sv = *reinterpret_cast<const uint16_t*>(ch + sb_off);
+                const uint32_t bv = *reinterpret_cast<const uint16_t*>(ch + sb_off + 256);
+                dequant_store4(cw, sv * 0x10001u, bv * 0x10001u, wdq + ws * kWdqBytes + row_off, r, 4 * hf);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) { mbar_arrive(&bars->raw_empty[rs]); mbar_arrive(&bars->a_full[as]); }
+                if (lane == 0) { mbar_arrive(&bars->raw_empty[rs]); mbar_arrive(&bars->wdq_full[ws]); }
+                if (threadIdx.x == 0) TRACE(TR_DDONE, rit);
                 ++rit;
-                ++ait;
             }
         }
         if (!ok && lane == 0) raise_abort(abort, p.status);
     } else {
-        // epilogue: acc[t][n] += w * y for every row of the tile
-        const int q = warp & 3, g = (warp - kDeqWarps) >> 2;
+        // epilogue: thread = token row (32 per warp, warp w % 4 = TMEM lane quadrant).  Its first
+        // thread waits for the accumulator and releases the 4 warps through a named barrier.
+        const int q = warp & 3;
         uint32_t use[2] = {0, 0}, tcount = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x, ++tcount) {
             const int4 t = p.tiles[tile];
-            const int e = t.x, row0 = t.y, rows = t.z, N = round16(t.z), mt = t.w;
+            const int e = t.x, row0 = t.y, rows = t.z, wt = t.w;
             const int buf = tcount & 1;
-            if (!warp_wait(&bars->tm_full[buf], use[buf] & 1, abort)) { ok = false; break; }
+            if (threadIdx.x == kDeqWarps * 32 && !mbar_wait(&bars->tm_full[buf], use[buf] & 1, abort))
+                raise_abort(abort, p.status);
+            named_bar_sync(2, kEpiWarps * 32);
+            if (*abort) { ok = false; break; }
             tc_fence_after();
-            const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-            const int n = mt * kTileRows + 32 * q + lane;
-            for (int c = g; c < N / 16; c += 2) {
-                uint32_t Y[16];
-                tmem_ld16(tmem + lane_base + 256u * buf + 16 * c, Y);
-                // token and weight of the 16 rows: lane jj fetches row 16c + jj
-                int my_t = 0;
-                float my_w = 0.f;
-                const int jl = 16 * c + (lane & 15);
-                if (jl < rows) {
-                    if (e < p.E) {
-                        const int asg = p.perm[row0 + jl];
-                        my_t = asg / p.k;
-                        my_w = p.topk_w[asg];
-                    } else {
-                        my_t = row0 + jl;
-                        my_w = 1.0f;
+            if (warp == kDeqWarps && lane == 0) TRACE(TR_ETILE, tcount);
+            const int tok = 32 * q + lane;                        // row within the tile
+            const bool live = tok < rows;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + 256u * buf;
+            if (!kDown) {
+                // columns 0..127: g for i = 128*wt + c; columns 128..255: u for the same i
+                const size_t hrow = e < p.E ? (size_t)row0 + tok : (size_t)p.k * p.T + row0 + tok;
+                uint16_t* hp = p.H + hrow * 2 * p.I + (size_t)wt * 128;
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t G[16], U[16];
+                    tmem_ld16(taddr + 16 * c, G);
+                    tmem_ld16(taddr + 128 + 16 * c, U);
+                    tmem_ld_wait();
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj += 2) {
+                        float hv[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const float gv = __uint_as_float(G[jj + u]), uv = __uint_as_float(U[jj + u]);
+                            hv[u] = gv / (1.0f + __expf(-gv)) * uv;
+                        }
+                        const uint32_t h2 = pack_bf16(hv[0], hv[1]);
+                        hi[jj / 2] = h2;
+                        lo[jj / 2] = pack_bf16(hv[0] - bf16lo(h2), hv[1] - bf16hi(h2));
+                    }
+                    if (live) {
+                        uint4* dh = reinterpret_cast<uint4*>(hp + 16 * c);
+                        uint4* dl = reinterpret_cast<uint4*>(hp + p.I + 16 * c);
+                        dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                        dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
                     }
                 }
-                tmem_ld_wait();
+            } else {
+                // 256 columns of d starting at 256*wt: acc[token][n] += w * y
+                int tk = 0;
+                float w = 0.f;
+                if (live) {
+                    if (e < p.E) {
+                        const int asg = p.perm[row0 + tok];
+                        tk = asg / p.k;
+                        w = p.topk_w[asg];
+                    } else {
+                        tk = row0 + tok;
+                        w = 1.0f;
+                    }
+                }
+                float* ap = p.acc + (size_t)tk * p.d + (size_t)wt * kWRows;
+                for (int c = 0; c < 16; ++c) {
+                    uint32_t Y[16];
+                    tmem_ld16(taddr + 16 * c, Y);
+                    tmem_ld_wait();
+                    if (live) {
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int tok = __shfl_sync(0xffffffffu, my_t, jj);
-                    const float w = __shfl_sync(0xffffffffu, my_w, jj);
-                    if (16 * c + jj < rows) atomicAdd(p.acc + (size_t)tok * p.d + n, w * __uint_as_float(Y[jj]));
+                        for (int v = 0; v < 4; ++v)
+                            atomicAdd(reinterpret_cast<float4*>(ap + 16 * c + 4 * v),
+                                      make_float4(w * __uint_as_float(Y[4 * v]), w * __uint_as_float(Y[4 * v + 1]),
+                                                  w * __uint_as_float(Y[4 * v + 2]), w * __uint_as_float(Y[4 * v + 3])));
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
+            if (warp == kDeqWarps && lane == 0) TRACE(TR_EDONE, tcount);
             if (lane == 0) mbar_arrive(&bars->tm_empty[buf]);
             use[buf]++;
         }
@@ -552,9 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void combine_kernel(const float4* __restrict__ acc, uint2* __restrict__ y, size_t n4) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         const float4 v = acc[i];
-        const uint32_t lo = (uint32_t)f32_to_bf16_rn(v.x) | ((uint32_t)f32_to_bf16_rn(v.y) << 16);
-        const uint32_t hi = (uint32_t)f32_to_bf16_rn(v.z) | ((uint32_t)f32_to_bf16_rn(v.w) << 16);
-        y[i] = make_uint2(lo, hi);
+        y[i] = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
     }
 }
 
@@ -569,43 +449,44 @@ FfnParams make_params(const FfnArgs& a, bool gate_up) {
     p.perm = a.perm;
     p.topk_w = a.topk_w;
     p.status = reinterpret_cast<int*>(a.ws + a.L.status);
+    p.trace = reinterpret_cast<unsigned long long*>(a.ws + a.L.dec);
     p.T = a.T; p.d = a.d; p.I = a.I; p.E = a.E; p.k = a.k;
     return p;
+}
+
+template <bool kDown>
+cudaError_t set_smem_attr() {
+    static bool done = false;
+    if (done) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(ffn_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           smem_bytes<kDown>());
+    if (err == cudaSuccess) done = true;
+    return err;
 }
 
 }  // namespace
 
 cudaError_t launch_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t err = cudaFuncSetAttribute(ffn_gate_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               GuPlan::bytes);
-        if (err != cudaSuccess) return err;
-        attr = true;
-    }
+    cudaError_t err = set_smem_attr<false>();
+    if (err != cudaSuccess) return err;
     CUtensorMap tm_xs, tm_x;
-    cudaError_t err = make_tmap_bf16_2d(&tm_xs, a.ws + a.L.xs, (uint64_t)a.k * a.T, a.d, (uint64_t)a.d * 2, kBK, kBoxRows);
+    err = make_tmap_bf16_2d(&tm_xs, a.ws + a.L.xs, (uint64_t)a.k * a.T, a.d, (uint64_t)a.d * 2, kBK, kTokRows);
     if (err != cudaSuccess) return err;
-    err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, kBoxRows);
+    err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, kTokRows);
     if (err != cudaSuccess) return err;
-    ffn_gate_up_kernel<<<a.num_sms, kThreads, GuPlan::bytes, st>>>(tm_xs, tm_x, make_params(a, true));
+    ffn_kernel<false><<<a.num_sms, kThreads, smem_bytes<false>(), st>>>(tm_xs, tm_x, make_params(a, true));
     *launches += 1;
     return cudaGetLastError();
 }
 
 cudaError_t launch_down(const FfnArgs& a, cudaStream_t st, unsigned long long* launches) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t err =
-            cudaFuncSetAttribute(ffn_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DnPlan::bytes);
-        if (err != cudaSuccess) return err;
-        attr = true;
-    }
-    CUtensorMap tm_h;
-    cudaError_t err = make_tmap_bf16_2d(&tm_h, a.ws + a.L.H, (uint64_t)(a.k + 1) * a.T, 2 * (uint64_t)a.I,
-                                        (uint64_t)a.I * 4, kBK, kBoxRows);
+    cudaError_t err = set_smem_attr<true>();
     if (err != cudaSuccess) return err;
-    ffn_down_kernel<<<a.num_sms, kThreads, DnPlan::bytes, st>>>(tm_h, make_params(a, false));
+    CUtensorMap tm_h;
+    err = make_tmap_bf16_2d(&tm_h, a.ws + a.L.H, (uint64_t)(a.k + 1) * a.T, 2 * (uint64_t)a.I, (uint64_t)a.I * 4,
+                            kBK, kTokRows);
+    if (err != cudaSuccess) return err;
+    ffn_kernel<true><<<a.num_sms, kThreads, smem_bytes<true>(), st>>>(tm_h, tm_h, make_params(a, false));
     *launches += 1;
     return cudaGetLastError();
 }

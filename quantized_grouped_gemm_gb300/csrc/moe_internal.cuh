@@ -24,8 +24,9 @@ namespace moe {
 //           ((word >> 4s) & 0x000F000F) is the consecutive pair (2s, 2s+1) for s = 0..3, each
 //           code sitting in the low mantissa bits of one bf16 half;
 //   scales  256 B = bf16 [128 rows];   biases 256 B = bf16 [128 rows].
-// Gate/up stacks interleave the gate chunk and the up chunk of the same (e, m, kb):
-//   [E][N/128][K/64][2][4608 B].  Down stacks: [E][N/128][K/64][4608 B].
+// Chunks come in pairs: gate/up stacks interleave the gate chunk and the up chunk of the same
+// (e, m, kb): [E][I/128][d/64][2][4608 B]; down stacks pair the two 128-row halves of a
+// 256-row tile: [E][d/256][I/64][2][4608 B].  One pair (9216 B) is one 256-row MMA operand.
 // ------------------------------------------------------------------------------------
 constexpr int kTileRows = 128;          // rows of a packed chunk = MMA M
 constexpr int kBK = 64;                 // columns of a packed chunk = one quant group
@@ -38,8 +39,9 @@ constexpr int kChunkPairBytes = 2 * kChunkBytes;
 // ------------------------------------------------------------------------------------
 struct WsLayout {
     size_t status;      // int32[64]: [0] status bits, [1] decode done-counter, [2..] per-tile counters
+    size_t logits;      // fp32 [T][E] router logits
     size_t blk;         // int32 [nblk][E] per-block counts, then per-block bases
-    size_t gu_tiles;    // int4 [max_gu]: (expert, row0, rows, mtile)
+    size_t gu_tiles;    // int4 [max_gu]: (expert, first row, rows, weight tile)
     size_t gu_num;      // int32
     size_t dn_tiles;    // int4 [max_dn]
     size_t dn_num;      // int32
@@ -52,7 +54,7 @@ struct WsLayout {
 };
 
 constexpr int kRouteBlockTokens = 32;   // tokens per routing block (one warp, one bitmask)
-constexpr int kMaxN = 256;              // max rows of a GEMM tile (MMA N)
+constexpr int kMaxN = 128;              // max token rows of a GEMM tile (MMA M)
 constexpr int kDecodeMaxT = 8;          // largest T the decode (GEMV) kernels take
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -69,9 +71,10 @@ inline WsLayout ws_layout(const moe_shape& s) {
     const int shared_nt = (T + kMaxN - 1) / kMaxN;
     const int routed_nt = gemm_ntile_bound(k * T, E);
     L.max_gu = (routed_nt + shared_nt) * (I / kTileRows);
-    L.max_dn = (routed_nt + shared_nt) * (d / kTileRows);
+    L.max_dn = (routed_nt + shared_nt) * (d / 256);
     size_t o = 0;
     L.status = o; o = align_up(o + 64 * 4, 256);
+    L.logits = o; o = align_up(o + (size_t)T * E * 4, 256);
     L.blk = o; o = align_up(o + (size_t)2 * L.nblk * E * 4, 256);
     L.gu_tiles = o; o = align_up(o + (size_t)L.max_gu * 16, 256);
     L.gu_num = o; o = align_up(o + 16, 256);
@@ -100,8 +103,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// A wait gives up after this long; the kernel then records MOE_STATUS_TIMEOUT and unwinds.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+// A wait gives up after this many SM cycles (about 2 s at 2 GHz); the kernel then records
+// MOE_STATUS_TIMEOUT and unwinds.  clock64 is cheap to read, unlike %globaltimer.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -120,11 +124,27 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase completes (or the hint
+// runs out) instead of spinning, so waiting warps leave the issue slots to working warps.
+constexpr uint32_t kSuspendHintNs = 1000000;   // 1 ms
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -132,18 +152,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Bounded spin (non-suspending test_wait) for single-thread roles, whose wake-up latency is
+// on the critical path.  Same contract as mbar_wait.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((++n & 255u) == 0) {
+            if (*abort) return false;
+            if (clock64() - t0 > kWaitLimitCycles) return false;
+        }
+    }
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false when the
 // wait ran out or another role of the CTA already aborted (*abort != 0).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    uint32_t n = 0;
+    const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((++n & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-        }
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) return false;
     }
 }
 
@@ -165,8 +197,26 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// Warm L2 with a contiguous range (16-byte multiple); no shared memory, no completion.
+__device__ __forceinline__ void prefetch_l2(const void* gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
+// Warm L2 with one tile of a 2-D tensor map.
+__device__ __forceinline__ void prefetch_l2_tile(const CUtensorMap* map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Hardware named barrier (ids 1..15; 0 is __syncthreads): waiting warps use no issue slots.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -5,6 +5,8 @@
 // bf16 scale and bias.  Output: one contiguous 4608-byte chunk per (expert, 128-row tile,
 // 64-column K block) holding codes (nibbles reordered so that a shift and a mask give two
 // consecutive codes in the mantissa of a bf16 pair), then the 128 scales and 128 biases.
+// Chunks are stored in pairs of 9216 bytes: the gate and the up chunk of the same rows, or
+// (down stacks) the two 128-row halves of a 256-row tile.
 // Still 4 bits per weight: no bf16 copy of the weights is made.
 #include "moe_internal.cuh"
 
@@ -26,7 +28,9 @@ __global__ void pack_kernel(int E, int N, int K, const uint8_t* __restrict__ cod
     const int e = (int)(rest / MT);
     const int row = mt * kTileRows + r;
     const uint8_t* src = codes + ((size_t)e * N + row) * (K / 2) + (size_t)kb * (kBK / 2);
-    uint8_t* chunk = dst + ((((size_t)e * MT + mt) * KB + kb) * nslots + slot) * kChunkBytes;
+    // nslots == 2, slot < 0: the two 128-row halves of a 256-row tile form the pair (down stacks)
+    const int tile = slot < 0 ? mt / 2 : mt, s = slot < 0 ? mt % 2 : slot, ntile = slot < 0 ? MT / 2 : MT;
+    uint8_t* chunk = dst + ((((size_t)e * ntile + tile) * KB + kb) * nslots + s) * kChunkBytes;
     constexpr int kPerm[8] = {0, 2, 4, 6, 1, 3, 5, 7};   // nibble p <- column offset kPerm[p]
 #pragma unroll
     for (int h = 0; h < 2; ++h)

@@ -8,12 +8,13 @@
 //   groups, and a block map lists the fixed-size tiles for the grouped GEMM -- all enqueued
 //   without a CPU stop inside the layer.
 //
-// Prefill (three launches):
-//   route_logits_topk  one CTA per 32-token block: router logits in the fixed fp32 order,
-//                      top-8 + weights, the block's per-expert counts.
+// Prefill (four launches):
+//   route_logits       CTA per (32-token block, 16 experts): router logits in the fixed
+//                      fp32 order.
+//   route_topk         one CTA per block: top-8 + weights, the block's per-expert counts.
 //   route_scan         one CTA: per-block bases, counts, offsets, the exported block map
 //                      and the GEMM tile lists (expert, first row, rows, 128-row M tile).
-//   route_scatter      one CTA per block: stable group positions (rank of the token among
+//   route_scatter      one CTA per (block, slot): stable group positions (rank of the token among
 //                      the block's tokens routed to the same expert, from a bitmask), perm /
 //                      pos, the gathered rows xs, and zeroing of the fp32 token-order sum.
 // Decode (one launch): route_decode -- a warp per expert logit, the last CTA to finish
@@ -75,100 +76,105 @@ __device__ __forceinline__ void warp_topk256(const float* lg, int k, int lane, i
 }
 
 // ---------------------------------------------------------------------------------------
-// route_logits_topk: grid = ceil(T/32) blocks of 256 threads.
+// route_logits: grid = (ceil(T/32) token blocks, 256/16 expert groups), 256 threads.
 // Lane l of every warp is partial sum l of the fixed order: it takes columns
-// k = 256*i + 8*l + j for i ascending, j = 0..7, with fmaf starting from 0.  A warp holds
-// a 4-token x 16-expert tile (64 accumulators per lane); the 32 partial sums of each logit
-// are then added by a recursive-halving exchange over lane distances 16, 8, 4, 2, 1 -- the
-// same pairing, hence the same value, as the tree s[i] += s[i+m].
+// k = 256*i + 8*l + j for i ascending, j = 0..7, with fmaf starting from 0.  Warp w holds
+// tokens 4w..4w+3 of the block x the CTA's 16 experts (64 accumulators per lane); the 32
+// partial sums of each logit are then added by a recursive-halving exchange over lane
+// distances 16, 8, 4, 2, 1 -- the same pairing, hence the same value, as the tree
+// s[i] += s[i+m].  Logits (+ bias) go to the workspace, [T][256] fp32.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kRouteThreads) route_logits_topk(RouteArgs a) {
-    __shared__ float s_lg[kRouteBlockTokens][256];
-    __shared__ int s_idx[kRouteBlockTokens][8];
+__global__ void __launch_bounds__(kRouteThreads) route_logits(RouteArgs a) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t0 = blockIdx.x * kRouteBlockTokens;
+    const int e0 = blockIdx.y * kExpPerPass;
+    const int d = a.d;
+    const int nI = d / 256;
+    float* logits = reinterpret_cast<float*>(a.ws + a.L.logits);
+
+    float acc[4][kExpPerPass];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int e = 0; e < kExpPerPass; ++e) acc[t][e] = 0.f;
+    for (int i = 0; i < nI; ++i) {
+        const int col = 256 * i + 8 * lane;
+        float xf[4][8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int tok = t0 + 4 * warp + t;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (tok < a.T) v = ld_nc_v4(a.x + (size_t)tok * d + col);
+            xf[t][0] = bf16lo(v.x); xf[t][1] = bf16hi(v.x); xf[t][2] = bf16lo(v.y); xf[t][3] = bf16hi(v.y);
+            xf[t][4] = bf16lo(v.z); xf[t][5] = bf16hi(v.z); xf[t][6] = bf16lo(v.w); xf[t][7] = bf16hi(v.w);
+        }
+#pragma unroll
+        for (int e = 0; e < kExpPerPass; ++e) {
+            uint4 v = ld_nc_v4(a.w_router + (size_t)(e0 + e) * d + col);
+            float wf[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
+                           bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int t = 0; t < 4; ++t) acc[t][e] = fmaf(xf[t][j], wf[j], acc[t][e]);
+        }
+    }
+    // recursive halving over 64 values (index o = 16*t + e); lane l ends with o = 2l, 2l+1
+    float v[64];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int e = 0; e < kExpPerPass; ++e) v[16 * t + e] = acc[t][e];
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        const int m = 16 >> step;
+        const int c = 64 >> step;        // live values before this step
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int q = 0; q < c / 2; ++q) {
+            const float lo = v[q], hi = v[q + c / 2];
+            const float send = upper ? lo : hi;
+            const float keep = upper ? hi : lo;
+            v[q] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int o = 2 * lane + r;
+        const int t = o >> 4, e = e0 + (o & 15);
+        const int tok = t0 + 4 * warp + t;
+        float lg = v[r];
+        if (a.bias) lg = lg + a.bias[e];
+        if (tok < a.T) logits[(size_t)tok * 256 + e] = lg;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// route_topk: grid = ceil(T/32) blocks, 256 threads: top-8 + weights per token (warp w does
+// tokens 4w..4w+3) and the block's per-expert counts.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kRouteThreads) route_topk(RouteArgs a) {
     __shared__ uint32_t s_mask[256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t0 = blockIdx.x * kRouteBlockTokens;
-    const int d = a.d;
-    const int nI = d / 256;
-
-    for (int pass = 0; pass < 256 / kExpPerPass; ++pass) {
-        float acc[4][kExpPerPass];
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-#pragma unroll
-            for (int e = 0; e < kExpPerPass; ++e) acc[t][e] = 0.f;
-        const int e0 = pass * kExpPerPass;
-        for (int i = 0; i < nI; ++i) {
-            const int col = 256 * i + 8 * lane;
-            float xf[4][8];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int tok = t0 + 4 * warp + t;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (tok < a.T) v = ld_nc_v4(a.x + (size_t)tok * d + col);
-                xf[t][0] = bf16lo(v.x); xf[t][1] = bf16hi(v.x); xf[t][2] = bf16lo(v.y); xf[t][3] = bf16hi(v.y);
-                xf[t][4] = bf16lo(v.z); xf[t][5] = bf16hi(v.z); xf[t][6] = bf16lo(v.w); xf[t][7] = bf16hi(v.w);
-            }
-#pragma unroll
-            for (int e = 0; e < kExpPerPass; ++e) {
-                uint4 v = ld_nc_v4(a.w_router + (size_t)(e0 + e) * d + col);
-                float wf[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
-                               bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) acc[t][e] = fmaf(xf[t][j], wf[j], acc[t][e]);
-            }
-        }
-        // recursive halving over 64 values (index o = 16*t + e); lane l ends with o = 2l, 2l+1
-        float v[64];
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-#pragma unroll
-            for (int e = 0; e < kExpPerPass; ++e) v[16 * t + e] = acc[t][e];
-#pragma unroll
-        for (int step = 0; step < 5; ++step) {
-            const int m = 16 >> step;
-            const int c = 64 >> step;        // live values before this step
-            const bool upper = (lane & m) != 0;
-#pragma unroll
-            for (int q = 0; q < c / 2; ++q) {
-                const float lo = v[q], hi = v[q + c / 2];
-                const float send = upper ? lo : hi;
-                const float keep = upper ? hi : lo;
-                v[q] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int o = 2 * lane + r;
-            const int t = o >> 4, e = e0 + (o & 15);
-            float lg = v[r];
-            if (a.bias) lg = lg + a.bias[e];
-            s_lg[4 * warp + t][e] = lg;
-        }
-    }
-    for (int e = threadIdx.x; e < 256; e += kRouteThreads) s_mask[e] = 0;
+    const float* logits = reinterpret_cast<const float*>(a.ws + a.L.logits);
+    s_mask[threadIdx.x] = 0;
     __syncthreads();
-
-    // top-k: warp w handles tokens 4w..4w+3
     for (int t = 0; t < 4; ++t) {
         const int tl = 4 * warp + t, tok = t0 + tl;
         if (tok >= a.T) break;
         int e;
         float w;
-        warp_topk256(s_lg[tl], a.k, lane, e, w);
+        warp_topk256(logits + (size_t)tok * 256, a.k, lane, e, w);
         if (lane < a.k) {
             a.topk_idx[(size_t)tok * a.k + lane] = e;
             a.topk_w[(size_t)tok * a.k + lane] = w;
-            s_idx[tl][lane] = e;
             atomicOr(&s_mask[e], 1u << tl);
         }
     }
     __syncthreads();
     int32_t* blk_counts = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
-    for (int e = threadIdx.x; e < 256; e += kRouteThreads)
-        blk_counts[(size_t)blockIdx.x * 256 + e] = __popc(s_mask[e]);
+    blk_counts[(size_t)blockIdx.x * 256 + threadIdx.x] = __popc(s_mask[threadIdx.x]);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -222,10 +228,11 @@ __global__ void __launch_bounds__(256) route_scan(RouteArgs a) {
     }
     if (e == E - 1) s_tot[0] = tbase + nt;
 
-    // GEMM tile lists: an expert's rows split into ceil(rows / 256) near-equal N tiles;
-    // each N tile is repeated for every 128-row M tile (M innermost).  The shared expert
+    // GEMM tile lists: an expert's rows split into ceil(rows / kMaxN) near-equal token blocks;
+    // each block is repeated for every weight tile (weight tile innermost, so the CTAs that
+    // run at the same time share the block's activation rows in L2).  The shared expert
     // (expert index E) comes first and covers token rows 0..T-1.
-    const int MTgu = a.I / kTileRows, MTdn = a.d / kTileRows;
+    const int MTgu = a.I / kTileRows, MTdn = a.d / 256;   // 128 gate+up row pairs; 256-row down tiles
     const int nn = (run + kMaxN - 1) / kMaxN;
     const int nsh = (a.T + kMaxN - 1) / kMaxN;
     const int nbase = block_exclusive_scan(nn, s_tmp);
@@ -246,10 +253,10 @@ __global__ void __launch_bounds__(256) route_scan(RouteArgs a) {
             r0 += rows;
         }
     }
-    if (e < nsh) {   // shared expert N tiles (nsh <= 256 for T <= 65536)
+    for (int i = e; i < nsh; i += E) {   // shared expert N tiles
         const int base_rows = a.T / nsh, rem = a.T % nsh;
-        const int r0 = e * base_rows + min(e, rem);
-        emit(e, E, r0, base_rows + (e < rem ? 1 : 0));
+        const int r0 = i * base_rows + min(i, rem);
+        emit(i, E, r0, base_rows + (i < rem ? 1 : 0));
     }
     __syncthreads();
     if (e == 0) {
@@ -261,13 +268,17 @@ __global__ void __launch_bounds__(256) route_scan(RouteArgs a) {
 }
 
 // ---------------------------------------------------------------------------------------
-// route_scatter: one CTA (256 threads) per 32-token block.
+// route_scatter: grid = (ceil(T/32) blocks, k slots), 256 threads.  Every CTA rebuilds the
+// block's expert bitmasks (bit t set when token t of the block picked the expert), which
+// give the stable rank of a token among the block's tokens routed to the same expert; CTA
+// (b, j) then writes pos / perm of slot j, copies those 32 rows into expert order
+// (xs[p] = x[t]) and clears 1/k of the block's rows of the fp32 token-order sum.
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) route_scatter(RouteArgs a) {
     __shared__ uint32_t s_mask[256];
-    __shared__ int s_pos[kRouteBlockTokens * 8];
+    __shared__ int s_pos[kRouteBlockTokens];
     const int E = 256, k = a.k;
-    const int t0 = blockIdx.x * kRouteBlockTokens;
+    const int t0 = blockIdx.x * kRouteBlockTokens, slot = blockIdx.y;
     const int ntok = min(kRouteBlockTokens, a.T - t0);
     const int32_t* blk_base = reinterpret_cast<const int32_t*>(a.ws + a.L.blk) + (size_t)a.L.nblk * E;
     int* status = reinterpret_cast<int*>(a.ws + a.L.status);
@@ -277,36 +288,38 @@ __global__ void __launch_bounds__(256) route_scatter(RouteArgs a) {
     int e = -1;
     if (tl < ntok) {
         e = a.topk_idx[(size_t)(t0 + tl) * k + j];
-        if (e < 0 || e >= E) { set_status(status, MOE_STATUS_BAD_EXPERT); e = -1; }
+        if (e < 0 || e >= E) { if (slot == 0) set_status(status, MOE_STATUS_BAD_EXPERT); e = -1; }
         else atomicOr(&s_mask[e], 1u << tl);
     }
     __syncthreads();
-    if (e >= 0) {
-        const int rank = __popc(s_mask[e] & ((1u << tl) - 1u));
-        const int p = blk_base[(size_t)blockIdx.x * E + e] + rank;
-        const int asg = (t0 + tl) * k + j;
-        a.pos[asg] = p;
-        a.perm[p] = asg;
-        s_pos[threadIdx.x] = p;
-    } else {
-        s_pos[threadIdx.x] = -1;
+    if (j == slot) {
+        int p = -1;
+        if (e >= 0) {
+            const int rank = __popc(s_mask[e] & ((1u << tl) - 1u));
+            p = blk_base[(size_t)blockIdx.x * E + e] + rank;
+            const int asg = (t0 + tl) * k + j;
+            a.pos[asg] = p;
+            a.perm[p] = asg;
+        }
+        s_pos[tl] = p;
     }
     __syncthreads();
-    // gather rows into expert order: xs[p] = x[t]
+    // gather this slot's rows into expert order: xs[p] = x[t]
     uint16_t* xs = reinterpret_cast<uint16_t*>(a.ws + a.L.xs);
     const int cpr = a.d / 8;                       // 16-byte chunks per row
-    const int total = ntok * 8 * cpr;
+    const int total = ntok * cpr;
     for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-        const int pr = idx / cpr, c = idx % cpr;
-        const int p = s_pos[pr];
+        const int r = idx / cpr, c = idx % cpr;
+        const int p = s_pos[r];
         if (p < 0) continue;
-        const uint4 v = ld_nc_v4(a.x + (size_t)(t0 + pr / 8) * a.d + 8 * c);
+        const uint4 v = ld_nc_v4(a.x + (size_t)(t0 + r) * a.d + 8 * c);
         *reinterpret_cast<uint4*>(xs + (size_t)p * a.d + 8 * c) = v;
     }
-    // clear the fp32 token-order sum of these tokens
+    // clear this CTA's share of the fp32 token-order sum of the block
     float4* acc = reinterpret_cast<float4*>(a.ws + a.L.acc) + (size_t)t0 * (a.d / 4);
     const int n4 = ntok * (a.d / 4);
-    for (int idx = threadIdx.x; idx < n4; idx += blockDim.x) acc[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int idx = slot * blockDim.x + threadIdx.x; idx < n4; idx += k * blockDim.x)
+        acc[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -406,10 +419,11 @@ __global__ void __launch_bounds__(128) route_decode(RouteArgs a) {
 
 cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned long long* launches) {
     const int nblk = a.L.nblk;
-    route_logits_topk<<<nblk, kRouteThreads, 0, st>>>(a);
+    route_logits<<<dim3(nblk, 256 / kExpPerPass), kRouteThreads, 0, st>>>(a);
+    route_topk<<<nblk, kRouteThreads, 0, st>>>(a);
     route_scan<<<1, 256, 0, st>>>(a);
-    route_scatter<<<nblk, 256, 0, st>>>(a);
-    *launches += 3;
+    route_scatter<<<dim3(nblk, a.k), 256, 0, st>>>(a);
+    *launches += 4;
     return cudaGetLastError();
 }
 
