@@ -183,6 +183,32 @@ int moe_read_status(void* workspace_dev, void* stream, int* status_out);
 /* Number of kernels this library has launched in this process (diagnostics). */
 unsigned long long moe_launch_count(void);
 
+/* Size of the device scratch array behind moe_forward_decode_static. */
+#define MOE_STATIC_SCRATCH_BYTES 131072
+
+/* Batch-1 decode forward (T = 1) that allocates nothing and takes no workspace.
+ * This call has no counterpart on the pages; it is here for callers that cannot provide
+ * scratch memory: a plugin that is handed only its input and output device pointers by a
+ * host program owning every allocation, or a service loop that must not allocate once it
+ * runs.  It computes what moe_forward computes for one token (routing into *routing, the
+ * layer output into y_dev [d] bf16) with its scratch in a fixed array of
+ * MOE_STATIC_SCRATCH_BYTES in the library's device memory, which every GPU that loads the
+ * library holds until the process exits.
+ * - Shapes whose scratch (about d*4 + 8*E*4 + 18*I*4 bytes) exceeds the array are rejected
+ *   with MOE_ERR_WORKSPACE; T != 1 gives MOE_ERR_UNSUPPORTED.  Other checks as moe_forward.
+ * - No cudaMalloc/cudaFree or allocating library call is made.  The first call on a device
+ *   looks up the array's device address (cudaGetSymbolAddress); make that first call before
+ *   any stream capture.
+ * - All calls share the array and it keeps the last call's contents; each call clears the
+ *   part that must start at zero.  Calls that overlap on the GPU (e.g. two streams at once)
+ *   race on it: serialise them.
+ * - Device-side status bits are not reported by this call (use moe_forward with a workspace
+ *   and moe_read_status for diagnostics). */
+int moe_forward_decode_static(const moe_shape* shape, const uint16_t* x_dev, const uint16_t* w_router_dev,
+                              const float* logit_bias_dev, const void* packed_routed_dev,
+                              const void* packed_shared_dev, const moe_routing* routing, uint16_t* y_dev,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

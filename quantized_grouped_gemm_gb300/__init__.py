@@ -21,7 +21,8 @@ from ._lib import (MOE_ERR_CUDA, MOE_ERR_DEVICE_STATUS, MOE_ERR_DEVICE_TIMEOUT, 
 
 __all__ = ["MoEError", "shape", "options", "Routing", "workspace", "moe_workspace_bytes", "moe_packed_bytes",
            "moe_pack_weights", "moe_route", "moe_grouped_ffn", "moe_ffn_gate_up", "moe_ffn_down", "moe_combine",
-           "moe_forward", "moe_read_status", "moe_check_shape", "moe_launch_count", "lib"]
+           "moe_forward", "moe_read_status", "moe_check_shape", "moe_launch_count", "moe_forward_decode_static",
+           "lib"]
 
 
 class MoEError(RuntimeError):
@@ -157,6 +158,16 @@ def moe_forward(shp, x, w_router, logit_bias, packed_routed, packed_shared, rout
     _check(lib().moe_forward(ctypes.byref(shp), _p(x), _p(w_router), _p(logit_bias), _p(packed_routed),
                              _p(packed_shared), routing.ref(), _p(ws), ws.numel(), _p(y), _o(opts), _s(stream)),
            "moe_forward")
+
+
+def moe_forward_decode_static(shp, x, w_router, logit_bias, packed_routed, packed_shared, routing: Routing, y,
+                              stream=None) -> None:
+    """One-token forward with no workspace: the scratch is a fixed device array inside the
+    library (see moe_forward_decode_static in include/moe.h).  For callers that cannot
+    allocate scratch memory; calls that overlap on the GPU race on the shared array."""
+    _check(lib().moe_forward_decode_static(ctypes.byref(shp), _p(x), _p(w_router), _p(logit_bias),
+                                           _p(packed_routed), _p(packed_shared), routing.ref(), _p(y), _s(stream)),
+           "moe_forward_decode_static")
 
 
 def moe_read_status(ws, stream=None):

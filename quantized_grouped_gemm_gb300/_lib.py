@@ -19,6 +19,7 @@ MOE_ERR_DEVICE_TIMEOUT = -5
 MOE_ERR_WORKSPACE = -6
 MOE_STATUS_BAD_EXPERT = 0x1
 MOE_STATUS_TIMEOUT = 0x2
+MOE_STATIC_SCRATCH_BYTES = 131072
 
 _P = ctypes.c_void_p
 
@@ -68,6 +69,7 @@ _SIG = {
                                    ctypes.POINTER(moe_options), _P]),
     "moe_read_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
     "moe_launch_count": (ctypes.c_ulonglong, []),
+    "moe_forward_decode_static": (ctypes.c_int, [_SPS, _P, _P, _P, _P, _P, ctypes.POINTER(moe_routing), _P, _P]),
 }
 
 _lib = None

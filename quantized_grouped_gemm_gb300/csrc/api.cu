@@ -10,6 +10,8 @@ namespace moe {
 
 static std::atomic<unsigned long long> g_launches{0};
 
+void count_launches(unsigned long long n) { g_launches += n; }
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);

@@ -1,0 +1,63 @@
+"""The batch-1 decode forward that allocates nothing (moe_forward_decode_static).
+
+It exists for callers that cannot provide scratch memory (a plugin handed only input and
+output device pointers by a host program that owns every allocation, or a loop that must not
+allocate once running): its scratch is a fixed array inside the library.  This file is
+collected last so that a run stopping at its first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_grouped_gemm_gb300 as moe
+from moe_workload import configs, gen
+from gpu_helpers import DeviceLayer, assert_output_close, routing_to_host, to_dev, y_to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def test_static_scratch_decode_matches_workspace_forward_two_calls():
+    wl = configs.custom_workload("noalloc_t1_d1024_i256", T=1, d=1024, I=256)
+    sh = wl.shape
+    lay = configs.make_layer(wl)
+    shp = moe.shape(1, sh.d, sh.E, sh.k, sh.I, sh.I_shared)
+    dl = DeviceLayer(shp, lay)
+    xs = gen.normal_bf16(wl.seed, 77, (2, sh.d))
+    for call in range(2):                       # two calls in a row share the static array
+        x = np.ascontiguousarray(xs[call:call + 1])
+        xd = to_dev(x)
+        rt_ws, rt_st = moe.Routing(1), moe.Routing(1)
+        ws = moe.workspace(shp)
+        y_ws = torch.empty(1, sh.d, dtype=torch.int16, device="cuda")
+        y_st = torch.empty(1, sh.d, dtype=torch.int16, device="cuda")
+        moe.moe_forward(shp, xd, dl.w_router, None, dl.packed_routed, dl.packed_shared, rt_ws, ws, y_ws)
+        moe.moe_forward_decode_static(shp, xd, dl.w_router, None, dl.packed_routed, dl.packed_shared, rt_st, y_st)
+        torch.cuda.synchronize()
+        a, b = routing_to_host(rt_st, 1), routing_to_host(rt_ws, 1)
+        for key in ("topk_idx", "counts", "offsets", "perm", "pos", "tiles"):
+            assert np.array_equal(a[key], b[key]), key
+        assert np.abs(a["topk_w"] - b["topk_w"]).max() <= 1e-5
+        assert_output_close(y_to_f64(y_st), y_to_f64(y_ws), f"static-scratch call {call}")
+        # and both against the oracle
+        ref = oracle.route(x, lay.w_router)
+        out = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared)
+        assert_output_close(y_to_f64(y_st), out, f"static-scratch call {call} vs oracle")
+
+
+def test_static_scratch_rejects_what_does_not_fit():
+    L = moe.lib()
+    rt = moe.Routing(1)
+    big = moe.shape(1, 7168, I=8192)          # scratch > MOE_STATIC_SCRATCH_BYTES
+    z = torch.zeros(16, dtype=torch.int16, device="cuda")
+    rc = L.moe_forward_decode_static(ctypes.byref(big), ctypes.c_void_p(z.data_ptr()), ctypes.c_void_p(z.data_ptr()),
+                                     None, ctypes.c_void_p(z.data_ptr()), ctypes.c_void_p(z.data_ptr()), rt.ref(),
+                                     ctypes.c_void_p(z.data_ptr()), None)
+    assert rc == moe.MOE_ERR_WORKSPACE
+    two = moe.shape(2, 1024, I=256)
+    rc = L.moe_forward_decode_static(ctypes.byref(two), ctypes.c_void_p(z.data_ptr()), ctypes.c_void_p(z.data_ptr()),
+                                     None, ctypes.c_void_p(z.data_ptr()), ctypes.c_void_p(z.data_ptr()), rt.ref(),
+                                     ctypes.c_void_p(z.data_ptr()), None)
+    assert rc == moe.MOE_ERR_UNSUPPORTED
