@@ -167,7 +167,7 @@ size_t moe_max_tiles(int T, int k, int E, int tile_rows) {
 
 size_t moe_packed_bytes(const moe_shape* s, int num_experts, int I) {
     if (moe_check_shape(s) != MOE_OK || num_experts <= 0 || I <= 0 || I % 128 != 0) return 0;
-    return (size_t)num_experts * (gate_up_bytes(*s, I) + down_bytes(*s, I));
+    return kPackHeader + (size_t)num_experts * (gate_up_bytes(*s, I) + down_bytes(*s, I));
 }
 
 int moe_pack_weights(const moe_shape* s, const moe_expert_weights* src, int I, void* dst, size_t dst_bytes,
@@ -184,11 +184,19 @@ int moe_pack_weights(const moe_shape* s, const moe_expert_weights* src, int I, v
     const int E = src->num_experts;
     if (dst_bytes < moe_packed_bytes(s, E, I)) return MOE_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint8_t* d8 = static_cast<uint8_t*>(dst);
+    uint8_t* hdr = static_cast<uint8_t*>(dst);
+    int* mode = reinterpret_cast<int*>(hdr);
+    uint8_t* d8 = hdr + kPackHeader;
     unsigned long long n = 0;
-    cudaError_t e = launch_pack(E, I, s->d, src->gate, 0, 2, d8, st, &n);
-    if (e == cudaSuccess) e = launch_pack(E, I, s->d, src->up, 1, 2, d8, st, &n);
-    if (e == cudaSuccess) e = launch_pack(E, s->d, I, src->down, -1, 2, d8 + (size_t)E * gate_up_bytes(*s, I), st, &n);
+    cudaError_t e = cudaMemsetAsync(hdr, 0, kPackHeader, st);
+    const size_t ngu = (size_t)E * I * (s->d / 64), ndn = (size_t)E * s->d * (I / 64);
+    if (e == cudaSuccess) e = launch_scale_check(ngu, src->gate.scales_dev, mode, st, &n);
+    if (e == cudaSuccess) e = launch_scale_check(ngu, src->up.scales_dev, mode, st, &n);
+    if (e == cudaSuccess) e = launch_scale_check(ndn, src->down.scales_dev, mode, st, &n);
+    if (e == cudaSuccess) e = launch_pack(E, I, s->d, src->gate, 0, 2, d8, mode, st, &n);
+    if (e == cudaSuccess) e = launch_pack(E, I, s->d, src->up, 1, 2, d8, mode, st, &n);
+    if (e == cudaSuccess)
+        e = launch_pack(E, s->d, I, src->down, -1, 2, d8 + (size_t)E * gate_up_bytes(*s, I), mode, st, &n);
     g_launches += n;
     return cuda_status(e);
 }
@@ -250,9 +258,6 @@ int moe_ffn_down(const moe_shape* s, const moe_routing* rt, const void* wr, cons
     if (is_decode(s, op)) {
         e = launch_decode_down(a, nullptr, static_cast<cudaStream_t>(stream), &n);
     } else {
-        // the down stack follows the gate/up stack inside each packed buffer
-        a.w_routed += (size_t)s->E * gate_up_bytes(*s, s->I);
-        a.w_shared += gate_up_bytes(*s, s->I_shared);
         e = launch_down(a, static_cast<cudaStream_t>(stream), &n);
     }
     g_launches += n;

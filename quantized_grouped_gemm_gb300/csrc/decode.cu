@@ -23,21 +23,25 @@ constexpr int kKbPerCta = 4;
 
 // 16 B of packed codes (32 weights, columns 0..31 of a half chunk) dequantised and dotted
 // with 32 fp32 activations.
+template <bool kDenorm>
 __device__ __forceinline__ float dot32(uint4 codes, uint32_t s2, uint32_t b2, const float* xv, float acc) {
     const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
-    constexpr uint32_t kMagic = 0x43004300u, kOne = 0x3F803F80u, kNeg128 = 0xC300C300u;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
+        uint32_t wv[4];
+        dequant_word<kDenorm>(words[q], s2, b2, wv);
 #pragma unroll
-        for (int sft = 0; sft < 4; ++sft) {
-            const uint32_t v = ((words[q] >> (4 * sft)) & 0x000F000Fu) | kMagic;
-            const uint32_t wv = bf16x2_fma(bf16x2_fma(v, kOne, kNeg128), s2, b2);
-            const int c = 8 * q + 2 * sft;
-            acc = fmaf(bf16lo(wv), xv[c], acc);
-            acc = fmaf(bf16hi(wv), xv[c + 1], acc);
+        for (int u = 0; u < 4; ++u) {
+            const int c = 8 * q + 2 * u;
+            acc = fmaf(bf16lo(wv[u]), xv[c], acc);
+            acc = fmaf(bf16hi(wv[u]), xv[c + 1], acc);
         }
     }
     return acc;
+}
+
+__device__ __forceinline__ float dot32m(bool denorm, uint4 codes, uint32_t s2, uint32_t b2, const float* xv, float acc) {
+    return denorm ? dot32<true>(codes, s2, b2, xv, acc) : dot32<false>(codes, s2, b2, xv, acc);
 }
 
 struct DecParams {
@@ -48,6 +52,8 @@ struct DecParams {
     const uint8_t* w_gu_shared;
     const uint8_t* w_dn_routed;
     const uint8_t* w_dn_shared;
+    const int* mode_routed;    // scale encoding of each packed buffer
+    const int* mode_shared;
     float* gu;          // [9][2][I]
     float* acc;         // [d]
     uint16_t* y;        // [d] or null
@@ -70,6 +76,7 @@ __global__ void __launch_bounds__(256) decode_gate_up(DecParams p) {
     const uint8_t* base = s < p.k ? p.w_gu_routed + (size_t)(e * MT + mt) * KB * kChunkPairBytes
                                   : p.w_gu_shared + (size_t)mt * KB * kChunkPairBytes;
     const int mat = threadIdx.x >> 7, r = threadIdx.x & 127;
+    const bool denorm = *(s < p.k ? p.mode_routed : p.mode_shared) == kScaleDenorm;
     // issue every load of this thread first
     uint4 c[kKbPerCta][2];
     uint32_t sb[kKbPerCta][2];
@@ -87,8 +94,8 @@ __global__ void __launch_bounds__(256) decode_gate_up(DecParams p) {
 #pragma unroll
     for (int q = 0; q < kKbPerCta; ++q) {
         const uint32_t s2 = sb[q][0] * 0x10001u, b2 = sb[q][1] * 0x10001u;
-        acc = dot32(c[q][0], s2, b2, xs + q * kBK, acc);
-        acc = dot32(c[q][1], s2, b2, xs + q * kBK + 32, acc);
+        acc = dot32m(denorm, c[q][0], s2, b2, xs + q * kBK, acc);
+        acc = dot32m(denorm, c[q][1], s2, b2, xs + q * kBK + 32, acc);
     }
     atomicAdd(p.gu + ((size_t)s * 2 + mat) * p.I + mt * kTileRows + r, acc);
 }
@@ -114,6 +121,7 @@ __global__ void __launch_bounds__(256) decode_down(DecParams p) {
                (size_t)(mt / 2) * KB * kChunkPairBytes + (mt % 2) * kChunkBytes;
     const int hf = threadIdx.x >> 7, r = threadIdx.x & 127;
     const int kb0 = hf * (KB / 2), nkb = KB / 2;
+    const bool denorm = *(s < p.k ? p.mode_routed : p.mode_shared) == kScaleDenorm;
     float acc = 0.f;
     if (base) {
         // h = silu(g) * u for this slot
@@ -142,8 +150,8 @@ __global__ void __launch_bounds__(256) decode_down(DecParams p) {
                 if (u < nq) {
                     const int kb = kb0 + q + u;
                     const uint32_t s2 = sb[u][0] * 0x10001u, b2 = sb[u][1] * 0x10001u;
-                    acc = dot32(c[u][0], s2, b2, hsm + kb * kBK, acc);
-                    acc = dot32(c[u][1], s2, b2, hsm + kb * kBK + 32, acc);
+                    acc = dot32m(denorm, c[u][0], s2, b2, hsm + kb * kBK, acc);
+                    acc = dot32m(denorm, c[u][1], s2, b2, hsm + kb * kBK + 32, acc);
                 }
             }
         }
@@ -174,12 +182,15 @@ DecParams make_dec_params(const FfnArgs& a, uint16_t* y) {
     p.x = a.x;
     p.topk_idx = a.topk_idx;
     p.topk_w = a.topk_w;
-    const size_t gu_bytes = (size_t)a.E * (a.I / kTileRows) * (a.d / kBK) * kChunkPairBytes;
-    p.w_gu_routed = a.w_routed;
-    p.w_dn_routed = a.w_routed + gu_bytes;
+    // packed buffer: header, gate/up pairs, down pairs
     const size_t gu_sh = (size_t)(a.I / kTileRows) * (a.d / kBK) * kChunkPairBytes;
-    p.w_gu_shared = a.w_shared;
-    p.w_dn_shared = a.w_shared + gu_sh;
+    const size_t gu_bytes = (size_t)a.E * gu_sh;
+    p.w_gu_routed = a.w_routed + kPackHeader;
+    p.w_dn_routed = a.w_routed + kPackHeader + gu_bytes;
+    p.w_gu_shared = a.w_shared + kPackHeader;
+    p.w_dn_shared = a.w_shared + kPackHeader + gu_sh;
+    p.mode_routed = reinterpret_cast<const int*>(a.w_routed);
+    p.mode_shared = reinterpret_cast<const int*>(a.w_shared);
     p.gu = reinterpret_cast<float*>(a.ws + a.L.dec) + kDecodeMaxT * 256;
     p.acc = reinterpret_cast<float*>(a.ws + a.L.acc);
     p.y = y;

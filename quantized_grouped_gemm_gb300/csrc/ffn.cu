@@ -38,19 +38,19 @@ constexpr int kWdqBytes = kWRows * 128;            // 256 rows x 64 bf16
 constexpr int kRawBytes = kChunkPairBytes;         // 9216
 
 #ifndef MOE_GU_RAW
-#define MOE_GU_RAW 8
+#define MOE_GU_RAW 4
 #endif
 #ifndef MOE_GU_WDQ
-#define MOE_GU_WDQ 3
+#define MOE_GU_WDQ 4
 #endif
 #ifndef MOE_GU_ACT
 #define MOE_GU_ACT 3
 #endif
 #ifndef MOE_DN_RAW
-#define MOE_DN_RAW 6
+#define MOE_DN_RAW 3
 #endif
 #ifndef MOE_DN_WDQ
-#define MOE_DN_WDQ 3
+#define MOE_DN_WDQ 4
 #endif
 #ifndef MOE_DN_ACT
 #define MOE_DN_ACT 4
@@ -68,7 +68,7 @@ struct Cfg {
 };
 
 struct Bars {
-    uint64_t raw_full[8], raw_empty[8], act_full[8], act_empty[8], wdq_full[4], wdq_empty[4];
+    uint64_t raw_full[8], raw_empty[8], act_full[8], act_empty[8], wdq_full[6], wdq_empty[6];
     uint64_t tm_full[2], tm_empty[2], drain;
     uint32_t tmem_slot;
     int abort;
@@ -101,6 +101,8 @@ enum { TR_PRAW = 0, TR_PACT, TR_DWAIT, TR_DDONE, TR_MWAIT, TR_MDONE, TR_ETILE, T
 struct FfnParams {
     const uint8_t* w_routed;   // packed stack: [E][tiles][K/64][2][4608]
     const uint8_t* w_shared;
+    const int* mode_routed;    // scale encoding of each packed buffer (header word)
+    const int* mode_shared;
     const int4* tiles;         // (expert, first row, rows, weight tile); expert == E: shared
     const int* num_tiles;
     uint16_t* H;               // [(k+1)T][2I] bf16, hi | lo
@@ -152,25 +154,14 @@ struct Cursor {
 };
 
 // -------- dequant of 32 weights (one half row of a packed chunk) into the swizzled layout ----
+template <bool kDenorm>
 __device__ __forceinline__ void dequant_store4(uint4 codes, uint32_t s2, uint32_t b2, uint8_t* row_dst, int r,
                                                int c0) {
     const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
-    constexpr uint32_t kMagic = 0x43004300u;   // bf16 pair (128, 128); low nibble = mantissa
-    constexpr uint32_t kOne = 0x3F803F80u;
-    constexpr uint32_t kNeg128 = 0xC300C300u;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const uint32_t w = words[q];
         uint32_t v[4];
-        v[0] = (w & 0x000F000Fu) | kMagic;
-        v[1] = ((w >> 4) & 0x000F000Fu) | kMagic;
-        v[2] = ((w >> 8) & 0x000F000Fu) | kMagic;
-        v[3] = ((w >> 12) & 0x000F000Fu) | kMagic;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t code = bf16x2_fma(v[u], kOne, kNeg128);   // exact: (128 + q) - 128
-            v[u] = bf16x2_fma(code, s2, b2);                          // one rounding
-        }
+        dequant_word<kDenorm>(words[q], s2, b2, v);
         const int c = c0 + q;
         const uint32_t addr = smem_u32(row_dst + ((c ^ (r & 7)) << 4));
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
@@ -315,7 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t row_off = (r >> 3) * 1024 + (r & 7) * 128;
         uint32_t rit = 0;
         bool ok = true;
+        const int mode_r = *p.mode_routed, mode_s = *p.mode_shared;
         for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
+            const bool denorm = (p.tiles[tile].x < p.E ? mode_r : mode_s) == kScaleDenorm;
             for (int kb = 0; kb < KB; ++kb) {
                 const int rs = rit % C::RAW, ws = rit % C::WDQ;
                 const bool got = mbar_wait(&bars->raw_full[rs], (rit / C::RAW) & 1, abort) &&
@@ -326,7 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint4 cw = *reinterpret_cast<const uint4*>(ch + code_off);
                 const uint32_t sv = *reinterpret_cast<const uint16_t*>(ch + sb_off);
                 const uint32_t bv = *reinterpret_cast<const uint16_t*>(ch + sb_off + 256);
-                dequant_store4(cw, sv * 0x10001u, bv * 0x10001u, wdq + ws * kWdqBytes + row_off, r, 4 * hf);
+                if (denorm)
+                    dequant_store4<true>(cw, sv * 0x10001u, bv * 0x10001u, wdq + ws * kWdqBytes + row_off, r, 4 * hf);
+                else
+                    dequant_store4<false>(cw, sv * 0x10001u, bv * 0x10001u, wdq + ws * kWdqBytes + row_off, r, 4 * hf);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) { mbar_arrive(&bars->raw_empty[rs]); mbar_arrive(&bars->wdq_full[ws]); }
@@ -440,8 +436,12 @@ __global__ void combine_kernel(const float4* __restrict__ acc, uint2* __restrict
 
 FfnParams make_params(const FfnArgs& a, bool gate_up) {
     FfnParams p{};
-    p.w_routed = a.w_routed;
-    p.w_shared = a.w_shared;
+    // packed buffer: header, gate/up pairs, down pairs
+    const size_t gu_bytes = (size_t)(a.I / kTileRows) * (a.d / kBK) * kChunkPairBytes;
+    p.w_routed = a.w_routed + kPackHeader + (gate_up ? 0 : (size_t)a.E * gu_bytes);
+    p.w_shared = a.w_shared + kPackHeader + (gate_up ? 0 : gu_bytes);
+    p.mode_routed = reinterpret_cast<const int*>(a.w_routed);
+    p.mode_shared = reinterpret_cast<const int*>(a.w_shared);
     p.tiles = reinterpret_cast<const int4*>(a.ws + (gate_up ? a.L.gu_tiles : a.L.dn_tiles));
     p.num_tiles = reinterpret_cast<const int*>(a.ws + (gate_up ? a.L.gu_num : a.L.dn_num));
     p.H = reinterpret_cast<uint16_t*>(a.ws + a.L.H);

@@ -28,6 +28,16 @@ namespace moe {
 // (e, m, kb): [E][I/128][d/64][2][4608 B]; down stacks pair the two 128-row halves of a
 // 256-row tile: [E][d/256][I/64][2][4608 B].  One pair (9216 B) is one 256-row MMA operand.
 // ------------------------------------------------------------------------------------
+// A packed buffer starts with a 256-byte header; int32 header[0] is the scale encoding of the
+// whole buffer:
+//   kScaleDenorm (0): every scale satisfies |s| < 2^-5 and is stored as S = s * 2^133 (exact).
+//     A code q placed in the low mantissa bits of a zero-exponent bf16 is the subnormal
+//     q * 2^-133, so fma.rn.bf16x2(code, S, bias) = bf16(s*q + bias) with one rounding.
+//   kScaleMagic (1): scales stored as is; codes go through the bf16 128 + q form and one
+//     exact subtraction of 128 first.
+constexpr int kPackHeader = 256;
+constexpr int kScaleDenorm = 0;
+constexpr int kScaleMagic = 1;
 constexpr int kTileRows = 128;          // rows of a packed chunk = MMA M
 constexpr int kBK = 64;                 // columns of a packed chunk = one quant group
 constexpr int kChunkCodes = 4096;
@@ -39,7 +49,8 @@ constexpr int kChunkPairBytes = 2 * kChunkBytes;
 // ------------------------------------------------------------------------------------
 struct WsLayout {
     size_t status;      // int32[64]: [0] status bits, [1] decode done-counter, [2..] per-tile counters
-    size_t logits;      // fp32 [T][E] router logits
+    size_t rpart;       // fp32 [KS][T][E] tensor-core partial router logits
+    size_t wnorm;       // fp32 [E] router weight row norms
     size_t blk;         // int32 [nblk][E] per-block counts, then per-block bases
     size_t gu_tiles;    // int4 [max_gu]: (expert, first row, rows, weight tile)
     size_t gu_num;      // int32
@@ -59,6 +70,9 @@ constexpr int kDecodeMaxT = 8;          // largest T the decode (GEMV) kernels t
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// K slices of the tensor-core router GEMM (partial sums, combined when picking candidates)
+inline int router_kslices(int d) { return d / 64 >= 16 ? 4 : (d / 64 >= 4 ? 2 : 1); }
+
 inline int gemm_ntile_bound(int rows_total, int groups) {
     // tiles of <= kMaxN rows, near-equal split per group: at most rows/kMaxN + groups
     return rows_total / kMaxN + groups + 1;
@@ -74,7 +88,8 @@ inline WsLayout ws_layout(const moe_shape& s) {
     L.max_dn = (routed_nt + shared_nt) * (d / 256);
     size_t o = 0;
     L.status = o; o = align_up(o + 64 * 4, 256);
-    L.logits = o; o = align_up(o + (size_t)T * E * 4, 256);
+    L.rpart = o; o = align_up(o + (size_t)router_kslices(d) * T * E * 4, 256);
+    L.wnorm = o; o = align_up(o + (size_t)E * 4, 256);
     L.blk = o; o = align_up(o + (size_t)2 * L.nblk * E * 4, 256);
     L.gu_tiles = o; o = align_up(o + (size_t)L.max_gu * 16, 256);
     L.gu_num = o; o = align_up(o + 16, 256);
@@ -300,6 +315,22 @@ __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v <
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16f(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
 
+// Eight weights of one packed 32-bit word (pairs (0,1) (2,3) (4,5) (6,7) as bf16x2) with the
+// per-row scale and bias pairs s2 / b2 of the buffer's scale encoding.
+template <bool kDenorm>
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&v)[4]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint32_t c = (u == 0 ? w : (w >> (4 * u))) & 0x000F000Fu;
+        if (kDenorm) {
+            v[u] = bf16x2_fma(c, s2, b2);                                   // q * 2^-133 * S + b
+        } else {
+            const uint32_t q = bf16x2_fma(c | 0x43004300u, 0x3F803F80u, 0xC300C300u);   // (128 + q) - 128
+            v[u] = bf16x2_fma(q, s2, b2);
+        }
+    }
+}
+
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
     uint16_t r;
     asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
@@ -343,8 +374,8 @@ struct FfnArgs {
     const int32_t* topk_idx;
     const float* topk_w;
     const int32_t* perm;
-    const uint8_t* w_routed;   // packed
-    const uint8_t* w_shared;   // packed
+    const uint8_t* w_routed;   // packed buffer (header first)
+    const uint8_t* w_shared;   // packed buffer (header first)
     uint8_t* ws;
     WsLayout L;
     int num_sms;
@@ -358,7 +389,9 @@ cudaError_t launch_combine(int T, int d, const float* acc, uint16_t* y, cudaStre
 cudaError_t launch_decode_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_decode_down(const FfnArgs& a, uint16_t* y, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_pack(int E, int N, int K, const moe_q4& m, int pair_slot, int pair_count, uint8_t* dst,
-                        cudaStream_t st, unsigned long long* launches);
+                        const int* mode, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_scale_check(size_t n, const uint16_t* scales, int* mode, cudaStream_t st,
+                               unsigned long long* launches);
 
 // Encodes 2-D bf16 tensor maps (host; driver entry point fetched through the runtime).
 cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,

@@ -5,6 +5,8 @@
 // bf16 scale and bias.  Output: one contiguous 4608-byte chunk per (expert, 128-row tile,
 // 64-column K block) holding codes (nibbles reordered so that a shift and a mask give two
 // consecutive codes in the mantissa of a bf16 pair), then the 128 scales and 128 biases.
+// The buffer starts with a 256-byte header holding the scale encoding (kScaleDenorm when every
+// scale of the stack has |s| < 2^-5: scales stored as s * 2^133; else kScaleMagic).
 // Chunks are stored in pairs of 9216 bytes: the gate and the up chunk of the same rows, or
 // (down stacks) the two 128-row halves of a 256-row tile.
 // Still 4 bits per weight: no bf16 copy of the weights is made.
@@ -13,9 +15,25 @@
 namespace moe {
 namespace {
 
+// Sets *mode to kScaleMagic if any scale is non-finite or has |s| >= 2^-5 (bf16 0x3D00).
+__global__ void scale_check_kernel(size_t n, const uint16_t* __restrict__ scales, int* mode) {
+    bool bad = false;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        bad |= (scales[i] & 0x7FFFu) >= 0x3D00u;
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(mode, kScaleMagic);
+}
+
+// bf16 bits of s * 2^133 (exact for |s| < 2^-5, the only case it is used for)
+__device__ __forceinline__ uint16_t scale_to_denorm(uint16_t s) {
+    float f = __uint_as_float((uint32_t)s << 16);
+    f = f * 0x1p64f;
+    f = f * 0x1p69f;
+    return (uint16_t)(__float_as_uint(f) >> 16);
+}
+
 __global__ void pack_kernel(int E, int N, int K, const uint8_t* __restrict__ codes,
                             const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases, int slot,
-                            int nslots, uint8_t* __restrict__ dst) {
+                            int nslots, uint8_t* __restrict__ dst, const int* __restrict__ mode) {
     const int MT = N / kTileRows, KB = K / kBK;
     const size_t total = (size_t)E * MT * KB * kTileRows;
     const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
@@ -45,19 +63,28 @@ __global__ void pack_kernel(int E, int N, int K, const uint8_t* __restrict__ cod
             *reinterpret_cast<uint32_t*>(chunk + h * 2048 + r * 16 + 4 * w) = D;
         }
     const size_t gi = ((size_t)e * N + row) * (K / kBK) + kb;
-    reinterpret_cast<uint16_t*>(chunk + kChunkCodes)[r] = scales[gi];
+    const uint16_t sc = scales[gi];
+    reinterpret_cast<uint16_t*>(chunk + kChunkCodes)[r] = *mode == kScaleDenorm ? scale_to_denorm(sc) : sc;
     reinterpret_cast<uint16_t*>(chunk + kChunkCodes + 256)[r] = biases[gi];
 }
 
 }  // namespace
 
-cudaError_t launch_pack(int E, int N, int K, const moe_q4& m, int slot, int nslots, uint8_t* dst, cudaStream_t st,
-                        unsigned long long* launches) {
+cudaError_t launch_scale_check(size_t n, const uint16_t* scales, int* mode, cudaStream_t st,
+                               unsigned long long* launches) {
+    const size_t blocks = (n + 255) / 256 < 2048 ? (n + 255) / 256 : 2048;
+    scale_check_kernel<<<(unsigned)blocks, 256, 0, st>>>(n, scales, mode);
+    *launches += 1;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack(int E, int N, int K, const moe_q4& m, int slot, int nslots, uint8_t* dst, const int* mode,
+                        cudaStream_t st, unsigned long long* launches) {
     const size_t total = (size_t)E * (N / kTileRows) * (K / kBK) * kTileRows;
     const int threads = 256;
     const size_t blocks = (total + threads - 1) / threads;
     pack_kernel<<<(unsigned)blocks, threads, 0, st>>>(E, N, K, m.codes_dev, m.scales_dev, m.biases_dev, slot, nslots,
-                                                       dst);
+                                                       dst, mode);
     *launches += 1;
     return cudaGetLastError();
 }

@@ -8,10 +8,12 @@
 //   groups, and a block map lists the fixed-size tiles for the grouped GEMM -- all enqueued
 //   without a CPU stop inside the layer.
 //
-// Prefill (four launches):
-//   route_logits       CTA per (32-token block, 16 experts): router logits in the fixed
-//                      fp32 order.
-//   route_topk         one CTA per block: top-8 + weights, the block's per-expert counts.
+// Prefill (five launches):
+//   router_wnorm       ||W_r[e]|| per expert (for the error bound below).
+//   router_tc          approximate logits on the tensor cores (tcgen05, K-sliced partials).
+//   route_certify_topk per token: an error bound picks the candidates that can be in the top-8
+//                      of the fixed-order logits; only those are recomputed exactly (CUDA
+//                      cores, fixed fp32 order) and ranked; weights; per-block counts.
 //   route_scan         one CTA: per-block bases, counts, offsets, the exported block map
 //                      and the GEMM tile lists (expert, first row, rows, 128-row M tile).
 //   route_scatter      one CTA per (block, slot): stable group positions (rank of the token among
@@ -25,7 +27,6 @@ namespace moe {
 namespace {
 
 constexpr int kRouteThreads = 256;   // 8 warps; warp w owns tokens 4w..4w+3 of the block
-constexpr int kExpPerPass = 16;
 
 // Order-preserving key: larger logit first, then lower expert index.  NaN counts as -inf
 // and -0 as +0 (they compare equal to +0).
@@ -76,112 +77,356 @@ __device__ __forceinline__ void warp_topk256(const float* lg, int k, int lane, i
 }
 
 // ---------------------------------------------------------------------------------------
-// route_logits: grid = (ceil(T/32) token blocks, 256/16 expert groups), 256 threads.
-// Lane l of every warp is partial sum l of the fixed order: it takes columns
-// k = 256*i + 8*l + j for i ascending, j = 0..7, with fmaf starting from 0.  Warp w holds
-// tokens 4w..4w+3 of the block x the CTA's 16 experts (64 accumulators per lane); the 32
-// partial sums of each logit are then added by a recursive-halving exchange over lane
-// distances 16, 8, 4, 2, 1 -- the same pairing, hence the same value, as the tree
-// s[i] += s[i+m].  Logits (+ bias) go to the workspace, [T][256] fp32.
+// Exact logit of (token row xrow, expert row wrow) in the fixed order, computed by one warp:
+// lane l is partial sum l (columns 256*i + 8*l + j, i ascending, j = 0..7, fmaf from 0); the
+// xor-shuffle tree over 16, 8, 4, 2, 1 pairs the same lanes as s[i] += s[i+m].  Every lane
+// returns the logit (+ bias).
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kRouteThreads) route_logits(RouteArgs a) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t0 = blockIdx.x * kRouteBlockTokens;
-    const int e0 = blockIdx.y * kExpPerPass;
-    const int d = a.d;
-    const int nI = d / 256;
-    float* logits = reinterpret_cast<float*>(a.ws + a.L.logits);
-
-    float acc[4][kExpPerPass];
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-#pragma unroll
-        for (int e = 0; e < kExpPerPass; ++e) acc[t][e] = 0.f;
-    for (int i = 0; i < nI; ++i) {
+__device__ __forceinline__ float warp_pinned_logit(const uint16_t* xrow, const uint16_t* wrow, int d, int lane,
+                                                   const float* bias_e) {
+    float p = 0.f;
+    for (int i = 0; i < d / 256; ++i) {
         const int col = 256 * i + 8 * lane;
-        float xf[4][8];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int tok = t0 + 4 * warp + t;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (tok < a.T) v = ld_nc_v4(a.x + (size_t)tok * d + col);
-            xf[t][0] = bf16lo(v.x); xf[t][1] = bf16hi(v.x); xf[t][2] = bf16lo(v.y); xf[t][3] = bf16hi(v.y);
-            xf[t][4] = bf16lo(v.z); xf[t][5] = bf16hi(v.z); xf[t][6] = bf16lo(v.w); xf[t][7] = bf16hi(v.w);
-        }
-#pragma unroll
-        for (int e = 0; e < kExpPerPass; ++e) {
-            uint4 v = ld_nc_v4(a.w_router + (size_t)(e0 + e) * d + col);
-            float wf[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
-                           bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-#pragma unroll
-                for (int t = 0; t < 4; ++t) acc[t][e] = fmaf(xf[t][j], wf[j], acc[t][e]);
-        }
-    }
-    // recursive halving over 64 values (index o = 16*t + e); lane l ends with o = 2l, 2l+1
-    float v[64];
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-#pragma unroll
-        for (int e = 0; e < kExpPerPass; ++e) v[16 * t + e] = acc[t][e];
-#pragma unroll
-    for (int step = 0; step < 5; ++step) {
-        const int m = 16 >> step;
-        const int c = 64 >> step;        // live values before this step
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int q = 0; q < c / 2; ++q) {
-            const float lo = v[q], hi = v[q + c / 2];
-            const float send = upper ? lo : hi;
-            const float keep = upper ? hi : lo;
-            v[q] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-        }
+        const uint4 xv = ld_nc_v4(xrow + col);
+        const uint4 wv = ld_nc_v4(wrow + col);
+        p = fmaf(bf16lo(xv.x), bf16lo(wv.x), p);
+        p = fmaf(bf16hi(xv.x), bf16hi(wv.x), p);
+        p = fmaf(bf16lo(xv.y), bf16lo(wv.y), p);
+        p = fmaf(bf16hi(xv.y), bf16hi(wv.y), p);
+        p = fmaf(bf16lo(xv.z), bf16lo(wv.z), p);
+        p = fmaf(bf16hi(xv.z), bf16hi(wv.z), p);
+        p = fmaf(bf16lo(xv.w), bf16lo(wv.w), p);
+        p = fmaf(bf16hi(xv.w), bf16hi(wv.w), p);
     }
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int o = 2 * lane + r;
-        const int t = o >> 4, e = e0 + (o & 15);
-        const int tok = t0 + 4 * warp + t;
-        float lg = v[r];
-        if (a.bias) lg = lg + a.bias[e];
-        if (tok < a.T) logits[(size_t)tok * 256 + e] = lg;
+    for (int m = 16; m >= 1; m >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, m);
+    if (bias_e) p = p + *bias_e;
+    return p;
+}
+
+// Same value with the token row already in registers (xv[i] = columns 256 i + 8 lane .. +7,
+// NI = d / 256 <= 8) and all loads of the expert row issued before the arithmetic.
+template <int NI>
+__device__ __forceinline__ float warp_pinned_logit_regs(const uint4 (&xv)[8], const uint16_t* wrow, int lane,
+                                                        const float* bias_e) {
+    uint4 wv[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) wv[i] = ld_nc_v4(wrow + 256 * i + 8 * lane);
+    float p = 0.f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        p = fmaf(bf16lo(xv[i].x), bf16lo(wv[i].x), p);
+        p = fmaf(bf16hi(xv[i].x), bf16hi(wv[i].x), p);
+        p = fmaf(bf16lo(xv[i].y), bf16lo(wv[i].y), p);
+        p = fmaf(bf16hi(xv[i].y), bf16hi(wv[i].y), p);
+        p = fmaf(bf16lo(xv[i].z), bf16lo(wv[i].z), p);
+        p = fmaf(bf16hi(xv[i].z), bf16hi(wv[i].z), p);
+        p = fmaf(bf16lo(xv[i].w), bf16lo(wv[i].w), p);
+        p = fmaf(bf16hi(xv[i].w), bf16hi(wv[i].w), p);
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, m);
+    if (bias_e) p = p + *bias_e;
+    return p;
+}
+
+__device__ __forceinline__ float pinned_logit_any(const uint4 (&xv)[8], const uint16_t* xrow, const uint16_t* wrow,
+                                                  int d, int lane, const float* bias_e) {
+    switch (d / 256) {
+        case 1: return warp_pinned_logit_regs<1>(xv, wrow, lane, bias_e);
+        case 2: return warp_pinned_logit_regs<2>(xv, wrow, lane, bias_e);
+        case 4: return warp_pinned_logit_regs<4>(xv, wrow, lane, bias_e);
+        case 8: return warp_pinned_logit_regs<8>(xv, wrow, lane, bias_e);
+        default: return warp_pinned_logit(xrow, wrow, d, lane, bias_e);
     }
 }
 
 // ---------------------------------------------------------------------------------------
-// route_topk: grid = ceil(T/32) blocks, 256 threads: top-8 + weights per token (warp w does
-// tokens 4w..4w+3) and the block's per-expert counts.
+// router_wnorm: ||W_r[e]||_2 (fp32) for every expert; one warp per expert.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kRouteThreads) route_topk(RouteArgs a) {
+__global__ void __launch_bounds__(128) router_wnorm(RouteArgs a) {
+    const int lane = threadIdx.x & 31, e = blockIdx.x * 4 + (threadIdx.x >> 5);
+    float s = 0.f;
+    for (int c = 8 * lane; c < a.d; c += 256) {
+        const uint4 v = ld_nc_v4(a.w_router + (size_t)e * a.d + c);
+        const float f[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
+                            bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s = fmaf(f[j], f[j], s);
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    if (lane == 0) reinterpret_cast<float*>(a.ws + a.L.wnorm)[e] = sqrtf(s);
+}
+
+// ---------------------------------------------------------------------------------------
+// router_tc: approximate logits on the tensor cores.  grid = (ceil(T/128) token blocks,
+// KS K-slices); CTA (b, s) computes the partial product of 128 tokens x all 256 experts over
+// its K slice (tcgen05.mma M=128 x N=256 x K=16, operands by TMA with 128-byte swizzle, fp32
+// accumulator in TMEM) and writes it to part[s][t][256].  Only used to pick candidates.
+// Warps: 0 producer, 1 MMA + TMEM owner, 2..5 epilogue (one token row per thread).
+// ---------------------------------------------------------------------------------------
+constexpr int kRtStages = 4;
+constexpr int kRtA = 128 * 128;   // 128 tokens x 64 bf16
+constexpr int kRtB = 256 * 128;   // 256 experts x 64 bf16
+constexpr int kRtSmem = kRtStages * (kRtA + kRtB) + 256 + 1024;
+
+__global__ void __launch_bounds__(192, 1)
+    router_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, RouteArgs a,
+              int KS) {
+    extern __shared__ uint8_t smem_dyn[];
+    const uint32_t s0 = smem_u32(smem_dyn);
+    uint8_t* smem = smem_dyn + ((1024u - (s0 & 1023u)) & 1023u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRtStages * (kRtA + kRtB));
+    uint64_t* empty = full + kRtStages;
+    uint64_t* tmfull = empty + kRtStages;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(tmfull + 1);
+    int* abortp = reinterpret_cast<int*>(tslot + 1);
+    volatile int* abort = abortp;
+    int* status = reinterpret_cast<int*>(a.ws + a.L.status);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KB = a.d / kBK, kb0 = blockIdx.y * KB / KS, kb1 = (blockIdx.y + 1) * KB / KS;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRtStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+        mbar_init(tmfull, 1);
+        *abortp = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) { tmem_alloc(tslot, 256); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm_w);
+            uint32_t it = 0;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int st = it % kRtStages;
+                if (!mbar_wait(&empty[st], ((it / kRtStages) & 1) ^ 1, abort)) {
+                    *abort = 1;
+                    set_status(status, MOE_STATUS_TIMEOUT);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[st], kRtA + kRtB);
+                uint8_t* dst = smem + st * (kRtA + kRtB);
+                tma_load_2d(dst, &tm_x, kb * kBK, blockIdx.x * 128, &full[st]);
+                tma_load_2d(dst + kRtA, &tm_w, kb * kBK, 0, &full[st]);
+            }
+            // every issued copy lands before the CTA can exit
+            int never = 0;
+            const uint32_t first = it > (uint32_t)kRtStages ? it - kRtStages : 0;
+            for (uint32_t i = first; i < it; ++i) mbar_wait(&full[i % kRtStages], (i / kRtStages) & 1, &never);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, 256);
+            const uint32_t base = smem_u32(smem);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int st = it % kRtStages;
+                if (!mbar_wait(&full[st], (it / kRtStages) & 1, abort)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t sa = base + st * (kRtA + kRtB);
+                    tc_mma_bf16(tmem, sw128_desc(sa + ks * 32), sw128_desc(sa + kRtA + ks * 32), idesc,
+                                (kb > kb0 || ks) ? 1u : 0u);
+                }
+                tc_commit(&empty[st]);
+            }
+            if (!ok) { *abort = 1; set_status(status, MOE_STATUS_TIMEOUT); }
+            tc_commit(tmfull);     // also drains every MMA before the epilogue / dealloc
+        }
+    } else {
+        const int q = warp & 3;
+        const bool got = mbar_wait(tmfull, 0, abort);
+        if (__all_sync(0xffffffffu, got)) {
+            tc_fence_after();
+            const int t = blockIdx.x * 128 + 32 * q + lane;
+            float* dst = reinterpret_cast<float*>(a.ws + a.L.rpart) + ((size_t)blockIdx.y * a.T + t) * 256;
+            for (int c = 0; c < 16; ++c) {
+                uint32_t v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * c, v);
+                tmem_ld_wait();
+                if (t < a.T) {
+                    float4* d4 = reinterpret_cast<float4*>(dst + 16 * c);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        d4[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                            __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+                }
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------------------
+// route_certify_topk: grid = ceil(T/32) blocks, 512 threads (warp w: tokens w, w + 16).
+// For each token, with l~[e] the tensor-core logit (sum of the K slices, + bias) and
+//   delta[e] = c * ||x_t|| * ||W_r[e]||,  c = 2 * ((d + 4 + 35) * 2^-23)  (+ a bias term),
+// which bounds |l~[e] - l[e]| for the fixed-order logit l (any fp32 summation of d exact
+// products errs by at most ~d*2^-23 * sum|x w| <= d*2^-23 ||x|| ||w||; the fixed order by
+// 69*2^-24 of the same; factor 2 for margin):
+//   lo = min over the 8 largest l~ of (l~[e] - delta[e]) <= the 8th largest l,
+// so every expert of the exact top-8 has l~[f] + delta[f] >= lo.  Those candidates (usually
+// ~10) are recomputed exactly (warp_pinned_logit) and ranked; over 32 candidates, all 256
+// are recomputed.  The result equals top-8 over all 256 exact logits.
+// Also writes the block's per-expert counts.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(512) route_certify_topk(RouteArgs a, int KS) {
     __shared__ uint32_t s_mask[256];
+    __shared__ float s_all[16][256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t0 = blockIdx.x * kRouteBlockTokens;
-    const float* logits = reinterpret_cast<const float*>(a.ws + a.L.logits);
-    s_mask[threadIdx.x] = 0;
+    const float* part = reinterpret_cast<const float*>(a.ws + a.L.rpart);
+    const float* wnorm = reinterpret_cast<const float*>(a.ws + a.L.wnorm);
+    const float c = 2.0f * (float)(a.d + 4 + 35) * 1.1920928955078125e-7f;   // 2^-23
+    if (threadIdx.x < 256) s_mask[threadIdx.x] = 0;
     __syncthreads();
-    for (int t = 0; t < 4; ++t) {
-        const int tl = 4 * warp + t, tok = t0 + tl;
-        if (tok >= a.T) break;
-        int e;
-        float w;
-        warp_topk256(logits + (size_t)tok * 256, a.k, lane, e, w);
+    for (int rep = 0; rep < 2; ++rep) {          // warp w: tokens w and w + 16 of the block
+    const int tl = warp + 16 * rep, tok = t0 + tl;
+    if (tok < a.T) {
+        const uint16_t* xrow = a.x + (size_t)tok * a.d;
+        // the token row in registers (first 8 column groups) and ||x_t||
+        uint4 xv[8];
+        float nx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            xv[i] = make_uint4(0, 0, 0, 0);
+            if (i < a.d / 256) xv[i] = ld_nc_v4(xrow + 256 * i + 8 * lane);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float f[8] = {bf16lo(xv[i].x), bf16hi(xv[i].x), bf16lo(xv[i].y), bf16hi(xv[i].y),
+                                bf16lo(xv[i].z), bf16hi(xv[i].z), bf16lo(xv[i].w), bf16hi(xv[i].w)};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) nx = fmaf(f[j], f[j], nx);
+        }
+        for (int col = 2048 + 8 * lane; col < a.d; col += 256) {
+            const uint4 v = ld_nc_v4(xrow + col);
+            const float f[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
+                                bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) nx = fmaf(f[j], f[j], nx);
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) nx += __shfl_xor_sync(0xffffffffu, nx, m);
+        nx = sqrtf(nx);
+        // approximate logits and their error bounds; lane holds experts lane + 32 s
+        float lt[8], dl[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int e = lane + 32 * s;
+            float v = 0.f;
+            for (int q = 0; q < KS; ++q) v += part[((size_t)q * a.T + tok) * 256 + e];
+            const float b = a.bias ? a.bias[e] : 0.f;
+            v += b;
+            lt[s] = v;
+            dl[s] = c * nx * wnorm[e] + 4.7683716e-7f * (fabsf(v) + fabsf(b) + 1.0f);   // + 2^-21 (|l|+|b|+1)
+        }
+        // lo = min over the 8 largest approximate logits of (l~ - delta)
+        unsigned long long key[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) key[s] = topk_key(lt[s], lane + 32 * s);
+        float lo = INFINITY;
+        for (int j = 0; j < 8; ++j) {
+            unsigned long long best = 0;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) best = key[s] > best ? key[s] : best;
+            best = warp_max_u64(best);
+            const int e = 0xFFFF - (int)(best & 0xFFFFu);
+            float v = 0.f;
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                if ((e & 31) == lane && (e >> 5) == s) { key[s] = 0; v = lt[s] - dl[s]; }
+            v = __shfl_sync(0xffffffffu, v, e & 31);
+            lo = fminf(lo, v);
+        }
+        // candidates, as one 256-bit mask held across the warp (word s in every lane)
+        uint32_t cm[8];
+        int ncand = 0;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const bool cand = !(lt[s] + dl[s] < lo);      // NaN-safe: NaN stays a candidate
+            cm[s] = __ballot_sync(0xffffffffu, cand);
+            ncand += __popc(cm[s]);
+        }
+        int e_out;
+        float w_out;
+        if (ncand <= 32) {
+            int my_e = -1;
+            float my_l = -INFINITY;
+            int j = 0;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                uint32_t m = cm[s];
+                while (m) {
+                    const int b = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int e = b + 32 * s;
+                    const float l = pinned_logit_any(xv, xrow, a.w_router + (size_t)e * a.d, a.d, lane,
+                                                     a.bias ? a.bias + e : nullptr);
+                    if (lane == j) { my_e = e; my_l = l; }
+                    ++j;
+                }
+            }
+            // top-k among the (<= 32) exact candidate logits, one per lane
+            unsigned long long k1 = my_e >= 0 ? topk_key(my_l, my_e) : 0ull;
+            int sel_e = -1;
+            float sel_l = 0.f, l0 = 0.f;
+            for (int jj = 0; jj < a.k; ++jj) {
+                const unsigned long long best = warp_max_u64(k1);
+                const int e = 0xFFFF - (int)(best & 0xFFFFu);
+                const int src = __ffs(__ballot_sync(0xffffffffu, my_e == e)) - 1;
+                const float l = __shfl_sync(0xffffffffu, my_l, src);
+                if (my_e == e) k1 = 0;
+                const float lc = (l != l) ? -INFINITY : l;
+                if (jj == 0) l0 = lc;
+                if (lane == jj) { sel_e = e; sel_l = lc; }
+            }
+            const float ex = lane < a.k ? expf(sel_l - l0) : 0.f;
+            float den = ex;
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) den += __shfl_xor_sync(0xffffffffu, den, m);
+            e_out = sel_e;
+            w_out = ex / den;
+        } else {
+            for (int e = 0; e < 256; ++e) {
+                const float l = pinned_logit_any(xv, xrow, a.w_router + (size_t)e * a.d, a.d, lane,
+                                                 a.bias ? a.bias + e : nullptr);
+                if (lane == (e & 31)) s_all[warp][e] = l;
+            }
+            __syncwarp();
+            warp_topk256(s_all[warp], a.k, lane, e_out, w_out);
+        }
         if (lane < a.k) {
-            a.topk_idx[(size_t)tok * a.k + lane] = e;
-            a.topk_w[(size_t)tok * a.k + lane] = w;
-            atomicOr(&s_mask[e], 1u << tl);
+            a.topk_idx[(size_t)tok * a.k + lane] = e_out;
+            a.topk_w[(size_t)tok * a.k + lane] = w_out;
+            atomicOr(&s_mask[e_out], 1u << tl);
         }
     }
+    }
     __syncthreads();
-    int32_t* blk_counts = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
-    blk_counts[(size_t)blockIdx.x * 256 + threadIdx.x] = __popc(s_mask[threadIdx.x]);
+    if (threadIdx.x < 256) {
+        int32_t* blk_counts = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
+        blk_counts[(size_t)blockIdx.x * 256 + threadIdx.x] = __popc(s_mask[threadIdx.x]);
+    }
 }
 
 // ---------------------------------------------------------------------------------------
-// route_scan: one CTA of 256 threads (thread e = expert e).
+// route_scan: one CTA of 1024 threads.  Thread (e, part) sums the counts of expert e over a
+// quarter of the token blocks; then per-block bases, counts, offsets (exclusive scan over
+// experts), the exported block map and the GEMM tile lists.
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ int block_exclusive_scan(int v, int* s_tmp) {
-    // 256 threads; s_tmp has 8 ints
+__device__ __forceinline__ int block_exclusive_scan256(int v, int* s_tmp) {
+    // called by the 256 threads of warps 0..7 only; s_tmp has 8 ints; uses named barrier 1
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int x = v;
 #pragma unroll
@@ -189,37 +434,72 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_tmp) {
         int y = __shfl_up_sync(0xffffffffu, x, m);
         if (lane >= m) x += y;
     }
-    __syncthreads();
+    named_bar_sync(1, 256);
     if (lane == 31) s_tmp[warp] = x;
-    __syncthreads();
+    named_bar_sync(1, 256);
     int base = 0;
     for (int w = 0; w < warp; ++w) base += s_tmp[w];
     return base + x - v;
 }
 
-__global__ void __launch_bounds__(256) route_scan(RouteArgs a) {
+__global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     __shared__ int s_tmp[8];
     __shared__ int s_tot[4];
-    const int e = threadIdx.x;
+    __shared__ int s_part[4][256];
+    __shared__ int s_off[256];
     const int E = 256;
+    const int e = threadIdx.x & 255, part = threadIdx.x >> 8;
     int32_t* blk_counts = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
     int32_t* blk_base = blk_counts + (size_t)a.L.nblk * E;
-    int run = 0;
-    for (int b = 0; b < a.L.nblk; ++b) {
-        const int c = blk_counts[(size_t)b * E + e];
-        blk_base[(size_t)b * E + e] = run;
-        run += c;
+    const int nb = a.L.nblk, nq = (nb + 3) / 4;
+    const int b0 = min(nb, part * nq), b1 = min(nb, b0 + nq);
+    int sum = 0;
+    {
+        int b = b0;
+        for (; b + 8 <= b1; b += 8) {
+            int c[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c[u] = blk_counts[(size_t)(b + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sum += c[u];
+        }
+        for (; b < b1; ++b) sum += blk_counts[(size_t)b * E + e];
     }
-    a.counts[e] = run;
-    const int off = block_exclusive_scan(run, s_tmp);
-    a.offsets[e] = off;
-    if (e == E - 1) a.offsets[E] = off + run;
-    for (int b = 0; b < a.L.nblk; ++b) blk_base[(size_t)b * E + e] += off;
+    s_part[part][e] = sum;
+    __syncthreads();
+    int pre = 0, run = 0;
+    for (int q = 0; q < 4; ++q) {
+        if (q < part) pre += s_part[q][e];
+        run += s_part[q][e];
+    }
+    if (part == 0) {
+        a.counts[e] = run;
+        const int off = block_exclusive_scan256(run, s_tmp);
+        s_off[e] = off;
+        a.offsets[e] = off;
+        if (e == E - 1) a.offsets[E] = off + run;
+    }
+    __syncthreads();
+    // per-block bases: offsets[e] + counts of e in earlier blocks
+    {
+        int r = s_off[e] + pre;
+        int b = b0;
+        for (; b + 8 <= b1; b += 8) {
+            int c[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c[u] = blk_counts[(size_t)(b + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) { blk_base[(size_t)(b + u) * E + e] = r; r += c[u]; }
+        }
+        for (; b < b1; ++b) { const int c = blk_counts[(size_t)b * E + e]; blk_base[(size_t)b * E + e] = r; r += c; }
+    }
+    if (part != 0) return;          // warps 8..31 are done; the rest uses named barrier 1 (256 threads)
+    const int off = s_off[e];
 
     // exported block map: ceil(count / tile_rows) tiles per expert, expert-ascending
     const int BM = a.tile_rows;
     const int nt = (run + BM - 1) / BM;
-    const int tbase = block_exclusive_scan(nt, s_tmp);
+    const int tbase = block_exclusive_scan256(nt, s_tmp);
     for (int i = 0; i < nt; ++i) {
         int32_t* tt = a.tiles + 3 * (size_t)(tbase + i);
         tt[0] = e;
@@ -235,9 +515,9 @@ __global__ void __launch_bounds__(256) route_scan(RouteArgs a) {
     const int MTgu = a.I / kTileRows, MTdn = a.d / 256;   // 128 gate+up row pairs; 256-row down tiles
     const int nn = (run + kMaxN - 1) / kMaxN;
     const int nsh = (a.T + kMaxN - 1) / kMaxN;
-    const int nbase = block_exclusive_scan(nn, s_tmp);
+    const int nbase = block_exclusive_scan256(nn, s_tmp);
     if (e == E - 1) s_tot[1] = nbase + nn;
-    __syncthreads();
+    named_bar_sync(1, 256);
     int4* gu = reinterpret_cast<int4*>(a.ws + a.L.gu_tiles);
     int4* dn = reinterpret_cast<int4*>(a.ws + a.L.dn_tiles);
     auto emit = [&](int slot, int ex, int r0, int rows) {
@@ -253,12 +533,11 @@ __global__ void __launch_bounds__(256) route_scan(RouteArgs a) {
             r0 += rows;
         }
     }
-    for (int i = e; i < nsh; i += E) {   // shared expert N tiles
+    for (int i = e; i < nsh; i += E) {   // shared expert token blocks
         const int base_rows = a.T / nsh, rem = a.T % nsh;
         const int r0 = i * base_rows + min(i, rem);
         emit(i, E, r0, base_rows + (i < rem ? 1 : 0));
     }
-    __syncthreads();
     if (e == 0) {
         *a.num_tiles = s_tot[0];
         const int total_n = nsh + s_tot[1];
@@ -418,12 +697,25 @@ __global__ void __launch_bounds__(128) route_decode(RouteArgs a) {
 }  // namespace
 
 cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned long long* launches) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t err = cudaFuncSetAttribute(router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+        if (err != cudaSuccess) return err;
+        attr = true;
+    }
     const int nblk = a.L.nblk;
-    route_logits<<<dim3(nblk, 256 / kExpPerPass), kRouteThreads, 0, st>>>(a);
-    route_topk<<<nblk, kRouteThreads, 0, st>>>(a);
-    route_scan<<<1, 256, 0, st>>>(a);
+    const int KS = router_kslices(a.d);
+    CUtensorMap tm_x, tm_w;
+    cudaError_t err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, 128);
+    if (err != cudaSuccess) return err;
+    err = make_tmap_bf16_2d(&tm_w, a.w_router, 256, a.d, (uint64_t)a.d * 2, kBK, 256);
+    if (err != cudaSuccess) return err;
+    router_wnorm<<<256 / 4, 128, 0, st>>>(a);
+    router_tc<<<dim3((a.T + 127) / 128, KS), 192, kRtSmem, st>>>(tm_x, tm_w, a, KS);
+    route_certify_topk<<<nblk, 512, 0, st>>>(a, KS);
+    route_scan<<<1, 1024, 0, st>>>(a);
     route_scatter<<<dim3(nblk, a.k), 256, 0, st>>>(a);
-    *launches += 4;
+    *launches += 5;
     return cudaGetLastError();
 }
 

@@ -57,8 +57,8 @@ def test_sizes(lib):
     # xs (8T x d bf16) + h (9T x 2I bf16) + fp32 sum (T x d) dominate
     assert ws >= 8 * 4096 * 2048 * 2 + 9 * 4096 * 1024 * 2 + 4096 * 2048 * 4
     assert ws < 1.1 * (8 * 4096 * 2048 * 2 + 9 * 4096 * 1024 * 2 + 4096 * 2048 * 4) + (1 << 20)
-    # packed bytes = checkpoint bytes: 0.5625 B per weight, 3 matrices of d x I per expert
-    assert lib.moe_packed_bytes(ctypes.byref(s), 256, 512) == 256 * 3 * 2048 * 512 * 9 // 16
+    # packed bytes = a 256-byte header + checkpoint bytes (0.5625 B per weight, 3 d x I matrices per expert)
+    assert lib.moe_packed_bytes(ctypes.byref(s), 256, 512) == 256 + 256 * 3 * 2048 * 512 * 9 // 16
     assert lib.moe_max_tiles(2048, 8, 256, 32) == 16384 // 32 + 256
     bad = _lib.moe_shape(4096, 2048, 256, 8, 500, 500, 64)
     assert lib.moe_workspace_bytes(ctypes.byref(bad), None) == 0

@@ -165,3 +165,75 @@ def test_bad_expert_index_sets_status_not_fault():
     rc, bits = moe.moe_read_status(ws)
     assert rc == moe.MOE_ERR_DEVICE_STATUS and bits & moe.MOE_STATUS_BAD_EXPERT
     assert moe.moe_read_status(ws)[0] == moe.MOE_OK      # cleared
+
+
+def _routing_case(wl, w_router, bias=None):
+    sh = wl.shape
+    lay = configs.make_layer(wl)
+    x = configs.make_x(wl)
+    shp = moe.shape(sh.T, sh.d, sh.E, sh.k, sh.I, sh.I_shared)
+    xd = to_dev(x)
+    rt = moe.Routing(sh.T)
+    ws = moe.workspace(shp)
+    moe.moe_route(shp, xd, to_dev(w_router), None if bias is None else to_dev(bias), rt, ws)
+    assert moe.moe_read_status(ws)[0] == moe.MOE_OK
+    ref = oracle.route(x, w_router, bias)
+    assert_routing_equal(routing_to_host(rt, sh.T), ref)
+    return ref
+
+
+def test_router_all_logits_equal_takes_full_recompute():
+    """Every router row identical: all 256 logits tie, more than 32 candidates, so the exact
+    logits of all experts are recomputed; ties go to the lower index."""
+    wl = configs.custom_workload("tie_t70_d512", T=70, d=512, I=128)
+    wr = configs.make_layer(wl).w_router.copy()
+    wr[:] = wr[3]
+    ref = _routing_case(wl, wr)
+    assert (ref["topk_idx"] == np.arange(8)).all()
+
+
+def test_router_duplicate_rows_exact_ties_at_the_boundary():
+    """Pairs of identical router rows give exact ties, some at the 8th/9th place."""
+    wl = configs.custom_workload("dup_t300_d1024", T=300, d=1024, I=128)
+    wr = configs.make_layer(wl).w_router.copy()
+    for a, b in [(1, 200), (17, 18), (40, 255), (100, 101), (7, 250)]:
+        wr[b] = wr[a]
+    _routing_case(wl, wr)
+
+
+def test_router_skew_bias_many_tokens_same_experts():
+    """The skewed workload's logit bias (a few experts take most rows)."""
+    wl = configs.WORKLOADS["skew_t16384_d2048"]
+    lay = configs.make_layer(wl)
+    sub = configs.custom_workload("skew_sub", T=1000, d=2048, I=512, seed=wl.seed)
+    ref = _routing_case(sub, lay.w_router, lay.logit_bias)
+    assert ref["counts"].max() > 300
+
+
+@pytest.mark.parametrize("T", [96, 1])
+def test_large_scales_use_the_exact_fallback_encoding(T):
+    """A stack with a scale >= 2^-5 cannot store scale * 2^133 in bf16; the packed buffer then
+    keeps scales as they are (header word 1) and the kernels dequantise through 128 + q."""
+    wl = configs.custom_workload(f"bigscale_t{T}", T=T, d=512, I=128)
+    sh = wl.shape
+    lay = configs.make_layer(wl)
+    big = np.uint16(0x3D80)                      # 0.0625 >= 2^-5
+    lay.routed.gate.scales[3, 5, 1] = big
+    lay.shared.down.scales[0, 7, 0] = big
+    x = configs.make_x(wl)
+    shp = moe.shape(T, sh.d, sh.E, sh.k, sh.I, sh.I_shared)
+    dl = DeviceLayer(shp, lay)
+    assert int(dl.packed_routed[:4].view(torch.int32).item()) == 1
+    assert int(dl.packed_shared[:4].view(torch.int32).item()) == 1
+    rt, ws, y = run_forward(shp, dl, to_dev(x))
+    ref = oracle.route(x, lay.w_router)
+    out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared)
+    assert_output_close(y_to_f64(y)[:T], out_ref, "fallback encoding")
+
+
+def test_default_scales_use_the_denormal_encoding():
+    wl = configs.custom_workload("smallscale", T=8, d=256, I=128)
+    sh = wl.shape
+    shp = moe.shape(8, sh.d, sh.E, sh.k, sh.I, sh.I_shared)
+    dl = DeviceLayer(shp, configs.make_layer(wl))
+    assert int(dl.packed_routed[:4].view(torch.int32).item()) == 0
