@@ -201,8 +201,9 @@ int moe_pack_weights(const moe_shape* s, const moe_expert_weights* src, int I, v
     return cuda_status(e);
 }
 
-int moe_route(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
-              const moe_routing* rt, void* ws, size_t ws_bytes, const moe_options* o, void* stream) {
+static int route_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
+                      const moe_routing* rt, void* ws, size_t ws_bytes, const moe_options* o, void* stream,
+                      const void* packed_shared) {
     int rc = moe_check_shape(s);
     if (rc != MOE_OK) return rc;
     Opts op;
@@ -213,11 +214,20 @@ int moe_route(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, c
     if (!x || !w_router || !aligned(x, 16) || !aligned(w_router, 16) || (bias && !aligned(bias, 4)))
         return MOE_ERR_INVALID_ARG;
     RouteArgs a = route_args(s, x, w_router, bias, rt, ws, op);
+    if (packed_shared) {   // decode: warm L2 with the shared expert's weights while routing
+        a.pf_ptr = static_cast<const uint8_t*>(packed_shared);
+        a.pf_bytes = moe_packed_bytes(s, 1, s->I_shared);
+    }
     unsigned long long n = 0;
     cudaError_t e = is_decode(s, op) ? launch_route_decode(a, static_cast<cudaStream_t>(stream), &n)
                                      : launch_route_prefill(a, static_cast<cudaStream_t>(stream), &n);
     g_launches += n;
     return cuda_status(e);
+}
+
+int moe_route(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
+              const moe_routing* rt, void* ws, size_t ws_bytes, const moe_options* o, void* stream) {
+    return route_impl(s, x, w_router, bias, rt, ws, ws_bytes, o, stream, nullptr);
 }
 
 static int ffn_common(const moe_shape* s, const uint16_t* x, const moe_routing* rt, const void* wr, const void* wsh,
@@ -292,10 +302,12 @@ int moe_combine(const moe_shape* s, const moe_routing* rt, void* ws, size_t ws_b
 int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias, const void* wr,
                 const void* wsh, const moe_routing* rt, void* ws, size_t ws_bytes, uint16_t* y, const moe_options* o,
                 void* stream) {
-    int rc = moe_route(s, x, w_router, bias, rt, ws, ws_bytes, o, stream);
-    if (rc != MOE_OK || s->T == 0) return rc;
     Opts op;
-    get_opts(o, &op);
+    int rc = get_opts(o, &op);
+    if (rc != MOE_OK) return rc;
+    const bool dec = s && is_decode(s, op) && wsh && aligned(wsh, 256);
+    rc = route_impl(s, x, w_router, bias, rt, ws, ws_bytes, o, stream, dec ? wsh : nullptr);
+    if (rc != MOE_OK || s->T == 0) return rc;
     if (is_decode(s, op)) {
         // decode: the down GEMV also writes y (its last CTA per row tile converts to bf16)
         rc = moe_ffn_gate_up(s, x, rt, wr, wsh, ws, ws_bytes, o, stream);

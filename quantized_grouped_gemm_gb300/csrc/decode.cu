@@ -68,26 +68,38 @@ __global__ void __launch_bounds__(256) decode_gate_up(DecParams p) {
     const int s = blockIdx.x / (MT * NKC);
     const int mt = (blockIdx.x / NKC) % MT;
     const int kc = blockIdx.x % NKC;
-    int e = p.E;
-    if (s < p.k) {
-        e = p.topk_idx[s];
-        if (e < 0 || e >= p.E) { if (threadIdx.x == 0) set_status(p.status, MOE_STATUS_BAD_EXPERT); return; }
-    }
-    const uint8_t* base = s < p.k ? p.w_gu_routed + (size_t)(e * MT + mt) * KB * kChunkPairBytes
-                                  : p.w_gu_shared + (size_t)mt * KB * kChunkPairBytes;
     const int mat = threadIdx.x >> 7, r = threadIdx.x & 127;
-    const bool denorm = *(s < p.k ? p.mode_routed : p.mode_shared) == kScaleDenorm;
-    // issue every load of this thread first
     uint4 c[kKbPerCta][2];
     uint32_t sb[kKbPerCta][2];
+    auto issue_loads = [&](const uint8_t* base) {
 #pragma unroll
-    for (int q = 0; q < kKbPerCta; ++q) {
-        const uint8_t* ch = base + (size_t)(kc * kKbPerCta + q) * kChunkPairBytes + mat * kChunkBytes;
-        c[q][0] = ld_nc_v4(ch + r * 16);
-        c[q][1] = ld_nc_v4(ch + 2048 + r * 16);
-        sb[q][0] = __ldg(reinterpret_cast<const uint16_t*>(ch + kChunkCodes) + r);
-        sb[q][1] = __ldg(reinterpret_cast<const uint16_t*>(ch + kChunkCodes + 256) + r);
+        for (int q = 0; q < kKbPerCta; ++q) {
+            const uint8_t* ch = base + (size_t)(kc * kKbPerCta + q) * kChunkPairBytes + mat * kChunkBytes;
+            c[q][0] = ld_nc_v4(ch + r * 16);
+            c[q][1] = ld_nc_v4(ch + 2048 + r * 16);
+            sb[q][0] = __ldg(reinterpret_cast<const uint16_t*>(ch + kChunkCodes) + r);
+            sb[q][1] = __ldg(reinterpret_cast<const uint16_t*>(ch + kChunkCodes + 256) + r);
+        }
+    };
+    int e = p.E;
+    if (s == p.k) {
+        // the shared expert's weights do not depend on routing: load them before waiting
+        issue_loads(p.w_gu_shared + (size_t)mt * KB * kChunkPairBytes);
+        pdl_wait();
+        pdl_launch_dependents();
+    } else {
+        pdl_wait();
+        pdl_launch_dependents();
+        e = p.topk_idx[s];
+        if (e < 0 || e >= p.E) { if (threadIdx.x == 0) set_status(p.status, MOE_STATUS_BAD_EXPERT); return; }
+        issue_loads(p.w_gu_routed + (size_t)(e * MT + mt) * KB * kChunkPairBytes);
+        // warm L2 with this expert's down weights for the next kernel (a slice per CTA)
+        const size_t dn_bytes = (size_t)(p.d / 256) * (p.I / kBK) * kChunkPairBytes;
+        const int part = mt * NKC + kc, nparts = MT * NKC;
+        const size_t lo = dn_bytes * part / nparts, hi = dn_bytes * (part + 1) / nparts;
+        prefetch_l2_range(p.w_dn_routed + (size_t)e * dn_bytes + lo, hi - lo, threadIdx.x, blockDim.x);
     }
+    const bool denorm = *(s < p.k ? p.mode_routed : p.mode_shared) == kScaleDenorm;
     xs[threadIdx.x] = bf16f(p.x[kc * kKbPerCta * kBK + threadIdx.x]);
     __syncthreads();
     float acc = 0.f;
@@ -106,6 +118,8 @@ __global__ void __launch_bounds__(256) decode_down(DecParams p) {
     __shared__ int s_last;
     const int MT = p.d / kTileRows, KB = p.I / kBK;
     const int s = blockIdx.x / MT, mt = blockIdx.x % MT;
+    pdl_wait();
+    pdl_launch_dependents();
     int e = p.E;
     float wgt = 1.0f;
     if (s < p.k) {
@@ -202,18 +216,32 @@ DecParams make_dec_params(const FfnArgs& a, uint16_t* y) {
 
 }  // namespace
 
+template <typename K>
+cudaError_t launch_pdl(K kernel, int grid, int block, size_t smem, cudaStream_t st, const DecParams& prm) {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 cudaError_t launch_decode_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches) {
     const int MT = a.I / kTileRows, NKC = a.d / kBK / kKbPerCta;
-    decode_gate_up<<<(a.k + 1) * MT * NKC, 256, 0, st>>>(make_dec_params(a, nullptr));
     *launches += 1;
-    return cudaGetLastError();
+    return launch_pdl(decode_gate_up, (a.k + 1) * MT * NKC, 256, 0, st, make_dec_params(a, nullptr));
 }
 
 cudaError_t launch_decode_down(const FfnArgs& a, uint16_t* y, cudaStream_t st, unsigned long long* launches) {
     const int MT = a.d / kTileRows;
-    decode_down<<<(a.k + 1) * MT, 256, a.I * sizeof(float), st>>>(make_dec_params(a, y));
     *launches += 1;
-    return cudaGetLastError();
+    return launch_pdl(decode_down, (a.k + 1) * MT, 256, a.I * sizeof(float), st, make_dec_params(a, y));
 }
 
 }  // namespace moe

@@ -345,6 +345,18 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 
 __device__ __forceinline__ void set_status(int* status, int bits) { atomicOr(status, bits); }
 
+// Programmatic dependent launch: wait for the previous grid's results / let the next grid start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Warm L2 with [p, p + bytes) split over the threads of a grid (each thread up to 4 KB pieces).
+__device__ __forceinline__ void prefetch_l2_range(const uint8_t* p, size_t bytes, size_t worker, size_t nworkers) {
+    for (size_t o = worker * 4096; o < bytes; o += nworkers * 4096) {
+        const uint32_t n = (uint32_t)(bytes - o < 4096 ? bytes - o : 4096) & ~15u;
+        if (n) prefetch_l2(p + o, n);
+    }
+}
+
 #endif  // __CUDACC__
 
 // ------------------------------------------------------------------------------------
@@ -366,6 +378,8 @@ struct RouteArgs {
     int I;
     uint8_t* ws;
     WsLayout L;
+    const uint8_t* pf_ptr;     // optional: weights to warm in L2 while routing (decode)
+    size_t pf_bytes;
 };
 
 struct FfnArgs {

@@ -26,7 +26,6 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteThreads = 256;   // 8 warps; warp w owns tokens 4w..4w+3 of the block
 
 // Order-preserving key: larger logit first, then lower expert index.  NaN counts as -inf
 // and -0 as +0 (they compare equal to +0).
@@ -615,24 +614,43 @@ __global__ void __launch_bounds__(128) route_decode(RouteArgs a) {
     const int d = a.d;
     float* logits = reinterpret_cast<float*>(a.ws + a.L.dec);
     int* status = reinterpret_cast<int*>(a.ws + a.L.status);
-    for (int t = 0; t < a.T; ++t) {
-        float p = 0.f;
-        for (int i = 0; i < d / 256; ++i) {
-            const int col = 256 * i + 8 * lane;
-            const uint4 xv = ld_nc_v4(a.x + (size_t)t * d + col);
-            const uint4 wv = ld_nc_v4(a.w_router + (size_t)e * d + col);
-            p = fmaf(bf16lo(xv.x), bf16lo(wv.x), p);
-            p = fmaf(bf16hi(xv.x), bf16hi(wv.x), p);
-            p = fmaf(bf16lo(xv.y), bf16lo(wv.y), p);
-            p = fmaf(bf16hi(xv.y), bf16hi(wv.y), p);
-            p = fmaf(bf16lo(xv.z), bf16lo(wv.z), p);
-            p = fmaf(bf16hi(xv.z), bf16hi(wv.z), p);
-            p = fmaf(bf16lo(xv.w), bf16lo(wv.w), p);
-            p = fmaf(bf16hi(xv.w), bf16hi(wv.w), p);
-        }
+    // Before the previous kernel's results are needed: this expert's router row (d <= 2048
+    // in registers) and an L2 warm-up of weights known in advance (the shared expert).
+    uint4 wv[8];
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, m);
-        if (a.bias) p = p + a.bias[e];
+    for (int i = 0; i < 8; ++i)
+        if (i < d / 256) wv[i] = ld_nc_v4(a.w_router + (size_t)e * d + 256 * i + 8 * lane);
+    if (a.pf_ptr) prefetch_l2_range(a.pf_ptr, a.pf_bytes, blockIdx.x * blockDim.x + threadIdx.x,
+                                    (size_t)gridDim.x * blockDim.x);
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int t = 0; t < a.T; ++t) {
+        const uint16_t* xrow = a.x + (size_t)t * d;
+        float p = 0.f;
+        if (d <= 2048) {
+            uint4 xv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < d / 256) xv[i] = ld_nc_v4(xrow + 256 * i + 8 * lane);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i < d / 256) {
+                    p = fmaf(bf16lo(xv[i].x), bf16lo(wv[i].x), p);
+                    p = fmaf(bf16hi(xv[i].x), bf16hi(wv[i].x), p);
+                    p = fmaf(bf16lo(xv[i].y), bf16lo(wv[i].y), p);
+                    p = fmaf(bf16hi(xv[i].y), bf16hi(wv[i].y), p);
+                    p = fmaf(bf16lo(xv[i].z), bf16lo(wv[i].z), p);
+                    p = fmaf(bf16hi(xv[i].z), bf16hi(wv[i].z), p);
+                    p = fmaf(bf16lo(xv[i].w), bf16lo(wv[i].w), p);
+                    p = fmaf(bf16hi(xv[i].w), bf16hi(wv[i].w), p);
+                }
+            }
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, m);
+            if (a.bias) p = p + a.bias[e];
+        } else {
+            p = warp_pinned_logit(xrow, a.w_router + (size_t)e * d, d, lane, a.bias ? a.bias + e : nullptr);
+        }
         if (lane == 0) logits[(size_t)t * 256 + e] = p;
     }
     __threadfence();
@@ -659,34 +677,53 @@ __global__ void __launch_bounds__(128) route_decode(RouteArgs a) {
         __syncwarp();
     }
     __syncthreads();
-    // metadata for T*k assignments (stable: token-ascending within an expert)
-    if (threadIdx.x == 0) {
-        const int n = a.T * a.k;
-        // offsets: exclusive scan over experts of the counts
-        int cnt[256];
-        for (int ex = 0; ex < 256; ++ex) cnt[ex] = 0;
-        for (int q = 0; q < n; ++q) cnt[s_e[q]]++;
-        int run = 0, nt = 0;
-        int start[256];
-        for (int ex = 0; ex < 256; ++ex) {
-            start[ex] = run;
-            a.offsets[ex] = run;
-            a.counts[ex] = cnt[ex];
-            for (int r = 0; r < cnt[ex]; r += a.tile_rows) {
-                int32_t* tt = a.tiles + 3 * (size_t)nt++;
-                tt[0] = ex; tt[1] = run + r; tt[2] = min(a.tile_rows, cnt[ex] - r);
-            }
-            run += cnt[ex];
-        }
-        a.offsets[256] = run;
-        *a.num_tiles = nt;
-        for (int q = 0; q < n; ++q) {       // q = t*k + j ascending: token-ascending per expert
-            const int p = start[s_e[q]]++;
-            a.pos[q] = p;
-            a.perm[p] = q;
-        }
-        *counter = 0;
+    // metadata for the n = T*k assignments, in parallel: expert e's group starts after every
+    // assignment to a lower expert; rows of a group are in assignment (= token) order.
+    __shared__ int s_cnt[256], s_tstart[256];
+    const int n = a.T * a.k;
+    for (int ex = threadIdx.x; ex < 256; ex += blockDim.x) {
+        int off = 0, cnt = 0;
+        for (int q = 0; q < n; ++q) { off += s_e[q] < ex; cnt += s_e[q] == ex; }
+        a.offsets[ex] = off;
+        a.counts[ex] = cnt;
+        s_cnt[ex] = cnt;
     }
+    if (threadIdx.x == 0) a.offsets[256] = n;
+    __syncthreads();
+    // block map: tiles of expert ex start after the tiles of lower experts
+    if (threadIdx.x < 32) {
+        int run = 0;
+        for (int base = 0; base < 256; base += 32) {
+            const int ex = base + threadIdx.x;
+            const int nt = (s_cnt[ex] + a.tile_rows - 1) / a.tile_rows;
+            int incl = nt;
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, m);
+                if ((int)threadIdx.x >= m) incl += y;
+            }
+            s_tstart[ex] = run + incl - nt;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (threadIdx.x == 0) *a.num_tiles = run;
+    }
+    __syncthreads();
+    for (int ex = threadIdx.x; ex < 256; ex += blockDim.x) {
+        int off = 0;
+        for (int q = 0; q < n; ++q) off += s_e[q] < ex;
+        for (int r = 0, i = 0; r < s_cnt[ex]; r += a.tile_rows, ++i) {
+            int32_t* tt = a.tiles + 3 * (size_t)(s_tstart[ex] + i);
+            tt[0] = ex; tt[1] = off + r; tt[2] = min(a.tile_rows, s_cnt[ex] - r);
+        }
+    }
+    if (threadIdx.x < n) {
+        const int q = threadIdx.x, ex = s_e[q];
+        int p = 0;
+        for (int q2 = 0; q2 < n; ++q2) p += (s_e[q2] < ex) || (s_e[q2] == ex && q2 < q);
+        a.pos[q] = p;
+        a.perm[p] = q;
+    }
+    if (threadIdx.x == 0) *counter = 0;
     // clear the decode accumulators (g/u per token and slot) and the token-order sum
     float* gu = logits + kDecodeMaxT * 256;
     for (int i = threadIdx.x; i < a.T * (a.k + 1) * 2 * a.I; i += blockDim.x) gu[i] = 0.f;
@@ -720,9 +757,18 @@ cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned l
 }
 
 cudaError_t launch_route_decode(const RouteArgs& a, cudaStream_t st, unsigned long long* launches) {
-    route_decode<<<64, 128, 0, st>>>(a);
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(64);
+    cfg.blockDim = dim3(128);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, route_decode, a);
     *launches += 1;
-    return cudaGetLastError();
+    return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace moe

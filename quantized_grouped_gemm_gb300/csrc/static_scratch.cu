@@ -91,6 +91,8 @@ extern "C" int moe_forward_decode_static(const moe_shape* s, const uint16_t* x, 
     ra.num_tiles = rt->num_tiles_dev;
     ra.ws = ws;
     ra.L = L;
+    ra.pf_ptr = static_cast<const uint8_t*>(packed_shared);   // warm L2 with the shared expert while routing
+    ra.pf_bytes = moe_packed_bytes(s, 1, s->I_shared);
     FfnArgs fa{};
     fa.T = 1; fa.d = s->d; fa.E = s->E; fa.k = s->k; fa.I = s->I;
     fa.x = x; fa.topk_idx = rt->topk_idx_dev; fa.topk_w = rt->topk_w_dev; fa.perm = rt->perm_dev;
