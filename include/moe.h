@@ -102,10 +102,15 @@ typedef struct moe_routing {
 } moe_routing;
 
 /* Options.  Zero-initialise and set what you need; zero fields take the defaults. */
+/* Values of moe_options.decode_path. */
+#define MOE_DECODE_AUTO 0   /* moe_forward with T = 1: one fused launch when it fits the GPU */
+#define MOE_DECODE_GEMV 1   /* always the three decode kernels (route, gate/up GEMV, down GEMV) */
+
 typedef struct moe_options {
     int tile_rows;          /* rows per exported block-map tile; default 32 */
     int decode_max_tokens;  /* T at or below this runs the decode (GEMV) kernels; default 1 */
-    int reserved[6];
+    int decode_path;        /* MOE_DECODE_AUTO (default) or MOE_DECODE_GEMV */
+    int reserved[5];
 } moe_options;
 
 /* Human-readable text for a return code. */
@@ -169,7 +174,18 @@ int moe_ffn_down(const moe_shape* shape, const moe_routing* routing, const void*
 int moe_combine(const moe_shape* shape, const moe_routing* routing, void* workspace_dev, size_t workspace_bytes,
                 uint16_t* y_dev, const moe_options* options, void* stream);
 
-/* The whole layer: moe_route, moe_grouped_ffn, moe_combine in one call. */
+/* The whole layer: moe_route, moe_grouped_ffn, moe_combine in one call.
+ * One token (T = 1, decode): with options.decode_path = MOE_DECODE_AUTO the layer is one
+ * kernel launch (routing, both projections and the combine) when I % 256 == 0 and all of its
+ * (k+1) * I/256 clusters of 8 CTAs fit on the GPU at once; otherwise the three decode kernels
+ * run.  Decode kernels are launched with programmatic dependent launch: they read
+ * w_router_dev, logit_bias_dev and the packed weights before the previous kernel on the
+ * stream has finished (x_dev and the workspace only after), so those inputs must not be
+ * written by the kernel launched just before this call on the same stream (moe_pack_weights
+ * ends with a memset, which orders a following launch after it).
+ * The one-launch kernel adds into the workspace's fp32 sum, which every completed moe_forward
+ * and moe_combine leaves at zero (moe_ffn_down without moe_combine does not).
+ * After a MOE_ERR_DEVICE_TIMEOUT the workspace counters are undefined: zero it again. */
 int moe_forward(const moe_shape* shape, const uint16_t* x_dev, const uint16_t* w_router_dev,
                 const float* logit_bias_dev, const void* packed_routed_dev, const void* packed_shared_dev,
                 const moe_routing* routing, void* workspace_dev, size_t workspace_bytes, uint16_t* y_dev,
@@ -194,8 +210,10 @@ unsigned long long moe_launch_count(void);
  * layer output into y_dev [d] bf16) with its scratch in a fixed array of
  * MOE_STATIC_SCRATCH_BYTES in the library's device memory, which every GPU that loads the
  * library holds until the process exits.
- * - Shapes whose scratch (about d*4 + 8*E*4 + 18*I*4 bytes) exceeds the array are rejected
- *   with MOE_ERR_WORKSPACE; T != 1 gives MOE_ERR_UNSUPPORTED.  Other checks as moe_forward.
+ * - Shapes whose scratch (256 + d*4 + 8*E*4 + 18*I*4 + 64*E bytes, each part rounded up to
+ *   256) exceeds the array are rejected with MOE_ERR_WORKSPACE, before any CUDA call;
+ *   T != 1 gives MOE_ERR_UNSUPPORTED.  Other checks as moe_forward; the one-launch kernel
+ *   runs when moe_forward would run it.
  * - No cudaMalloc/cudaFree or allocating library call is made.  The first call on a device
  *   looks up the array's device address (cudaGetSymbolAddress); make that first call before
  *   any stream capture.

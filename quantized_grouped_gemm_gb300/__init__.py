@@ -45,8 +45,12 @@ def shape(T: int, d: int, E: int = 256, k: int = 8, I: int = 512, I_shared: Opti
     return _lib.moe_shape(T, d, E, k, I, I if I_shared is None else I_shared, group)
 
 
-def options(tile_rows: int = 32, decode_max_tokens: int = 1) -> _lib.moe_options:
-    return _lib.moe_options(tile_rows, decode_max_tokens)
+DECODE_AUTO, DECODE_GEMV = 0, 1
+
+
+def options(tile_rows: int = 32, decode_max_tokens: int = 1, decode_path: int = DECODE_AUTO) -> _lib.moe_options:
+    """decode_path: DECODE_AUTO (one fused launch per token when it fits) or DECODE_GEMV."""
+    return _lib.moe_options(tile_rows, decode_max_tokens, decode_path)
 
 
 def _p(t: Optional[torch.Tensor]):

@@ -63,6 +63,7 @@ static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 struct Opts {
     int tile_rows = 32;
     int decode_max_tokens = 1;
+    int decode_path = MOE_DECODE_AUTO;
 };
 
 static int get_opts(const moe_options* o, Opts* out) {
@@ -72,6 +73,8 @@ static int get_opts(const moe_options* o, Opts* out) {
         if (o->tile_rows > 0) r.tile_rows = o->tile_rows;
         if (o->decode_max_tokens > 1) return MOE_ERR_UNSUPPORTED;
         r.decode_max_tokens = o->decode_max_tokens;
+        if (o->decode_path != MOE_DECODE_AUTO && o->decode_path != MOE_DECODE_GEMV) return MOE_ERR_INVALID_ARG;
+        r.decode_path = o->decode_path;
     }
     *out = r;
     return MOE_OK;
@@ -197,6 +200,9 @@ int moe_pack_weights(const moe_shape* s, const moe_expert_weights* src, int I, v
     if (e == cudaSuccess) e = launch_pack(E, I, s->d, src->up, 1, 2, d8, mode, st, &n);
     if (e == cudaSuccess)
         e = launch_pack(E, s->d, I, src->down, -1, 2, d8 + (size_t)E * gate_up_bytes(*s, I), mode, st, &n);
+    // a memset last: a kernel launched next with programmatic dependent launch (the decode
+    // kernels read weights before their wait) is then ordered after the packs, not overlapped
+    if (e == cudaSuccess) e = cudaMemsetAsync(hdr + 4, 0, 4, st);
     g_launches += n;
     return cuda_status(e);
 }
@@ -305,6 +311,37 @@ int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
     Opts op;
     int rc = get_opts(o, &op);
     if (rc != MOE_OK) return rc;
+    if (s && s->T == 1 && is_decode(s, op) && op.decode_path == MOE_DECODE_AUTO) {
+        // one launch for the whole token when the shape and the GPU allow it
+        if ((rc = moe_check_shape(s)) != MOE_OK) return rc;
+        if ((rc = check_routing(rt)) != MOE_OK) return rc;
+        if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
+        if (!x || !w_router || !wr || !wsh || !y || !aligned(x, 16) || !aligned(w_router, 16) ||
+            (bias && !aligned(bias, 4)) || !aligned(wr, 256) || !aligned(wsh, 256) || !aligned(y, 16))
+            return MOE_ERR_INVALID_ARG;
+        const WsLayout L = ws_layout(*s);
+        uint8_t* w8 = static_cast<uint8_t*>(ws);
+        FusedDecodeArgs fa{};
+        fa.d = s->d; fa.E = s->E; fa.k = s->k; fa.I = s->I;
+        fa.x = x; fa.w_router = w_router; fa.bias = bias;
+        fa.w_routed = static_cast<const uint8_t*>(wr);
+        fa.w_shared = static_cast<const uint8_t*>(wsh);
+        fa.topk_idx = rt->topk_idx_dev; fa.topk_w = rt->topk_w_dev; fa.counts = rt->counts_dev;
+        fa.offsets = rt->offsets_dev; fa.perm = rt->perm_dev; fa.pos = rt->pos_dev; fa.tiles = rt->tiles_dev;
+        fa.num_tiles = rt->num_tiles_dev;
+        fa.status = reinterpret_cast<int*>(w8 + L.status);
+        fa.logit_words = reinterpret_cast<unsigned long long*>(w8 + L.fzlog);
+        fa.acc = reinterpret_cast<float*>(w8 + L.acc);
+        fa.y = y;
+#ifdef MOE_TRACE
+        fa.trace = reinterpret_cast<unsigned long long*>(w8 + L.trace);
+#endif
+        unsigned long long n = 0;
+        cudaError_t e = launch_decode_fused(fa, static_cast<cudaStream_t>(stream), &n);
+        g_launches += n;
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+        // otherwise the three decode kernels below
+    }
     const bool dec = s && is_decode(s, op) && wsh && aligned(wsh, 256);
     rc = route_impl(s, x, w_router, bias, rt, ws, ws_bytes, o, stream, dec ? wsh : nullptr);
     if (rc != MOE_OK || s->T == 0) return rc;

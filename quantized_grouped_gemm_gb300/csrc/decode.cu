@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(256) decode_down(DecParams p) {
     if (threadIdx.x < kTileRows) {
         const float v = __ldcg(p.acc + mt * kTileRows + threadIdx.x);
         p.y[mt * kTileRows + threadIdx.x] = f32_to_bf16_rn(v);
+        p.acc[mt * kTileRows + threadIdx.x] = 0.f;   // leave the sum at zero
     }
     if (threadIdx.x == 0) p.tile_counters[mt] = 0;
 }

@@ -427,10 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ======================================================================================
 // combine: y = bf16(acc)
 // ======================================================================================
-__global__ void combine_kernel(const float4* __restrict__ acc, uint2* __restrict__ y, size_t n4) {
+// y = bf16(sum); the sum is left at zero (the one-launch decode kernel relies on that)
+__global__ void combine_kernel(float4* __restrict__ acc, uint2* __restrict__ y, size_t n4) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         const float4 v = acc[i];
         y[i] = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -494,7 +496,7 @@ cudaError_t launch_down(const FfnArgs& a, cudaStream_t st, unsigned long long* l
 cudaError_t launch_combine(int T, int d, const float* acc, uint16_t* y, cudaStream_t st, unsigned long long* launches) {
     const size_t n4 = (size_t)T * d / 4;
     const int blocks = (int)((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096);
-    combine_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(acc), reinterpret_cast<uint2*>(y), n4);
+    combine_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<float4*>(const_cast<float*>(acc)), reinterpret_cast<uint2*>(y), n4);
     *launches += 1;
     return cudaGetLastError();
 }

@@ -60,6 +60,8 @@ struct WsLayout {
     size_t H;           // bf16 [(k+1)*T][2*I] (hi | lo)
     size_t acc;         // fp32 [T][d] token-order sum
     size_t dec;         // decode scratch: logits fp32 [8][E], g/u fp32 [8][k+1][2][I]
+    size_t fzlog;       // u64 [8][E]: tagged logits of the one-launch decode kernel (eight copies)
+    size_t trace;       // tuning builds (MOE_TRACE): 64 KB of phase timestamps
     size_t total;
     int nblk, max_gu, max_dn;
 };
@@ -76,6 +78,12 @@ inline int router_kslices(int d) { return d / 64 >= 16 ? 4 : (d / 64 >= 4 ? 2 : 
 inline int gemm_ntile_bound(int rows_total, int groups) {
     // tiles of <= kMaxN rows, near-equal split per group: at most rows/kMaxN + groups
     return rows_total / kMaxN + groups + 1;
+}
+
+// Decode scratch of the GEMV kernels: router logits fp32 [8][E], g/u sums fp32 [8][k+1][2][I].
+inline size_t decode_scratch_bytes(int d, int E, int k, int I) {
+    (void)d;
+    return (size_t)kDecodeMaxT * E * 4 + (size_t)kDecodeMaxT * (k + 1) * 2 * I * 4;
 }
 
 inline WsLayout ws_layout(const moe_shape& s) {
@@ -98,7 +106,11 @@ inline WsLayout ws_layout(const moe_shape& s) {
     L.xs = o; o = align_up(o + (size_t)k * T * d * 2 + 256 * d * 2, 1024);
     L.H = o; o = align_up(o + (size_t)(k + 1) * T * 2 * I * 2 + 256 * 2 * I * 2, 1024);
     L.acc = o; o = align_up(o + (size_t)T * d * 4, 256);
-    L.dec = o; o = align_up(o + (size_t)kDecodeMaxT * E * 4 + (size_t)kDecodeMaxT * (k + 1) * 2 * I * 4, 256);
+    L.dec = o; o = align_up(o + decode_scratch_bytes(d, E, k, I), 256);
+    L.fzlog = o; o = align_up(o + (size_t)8 * E * 8, 256);
+#ifdef MOE_TRACE
+    L.trace = o; o += 65536;
+#endif
     L.total = o;
     return L;
 }
@@ -349,6 +361,123 @@ __device__ __forceinline__ void set_status(int* status, int bits) { atomicOr(sta
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Order-preserving key: larger logit first, then lower expert index.  NaN counts as -inf
+// and -0 as +0 (they compare equal to +0).
+__device__ __forceinline__ unsigned long long topk_key(float v, int e) {
+    if (v != v) v = -INFINITY;
+    if (v == 0.0f) v = 0.0f;
+    uint32_t u = __float_as_uint(v);
+    uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)o << 32) | (uint32_t)(0xFFFFu - (uint32_t)e);
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        unsigned long long o = __shfl_xor_sync(0xffffffffu, v, m);
+        v = o > v ? o : v;
+    }
+    return v;
+}
+
+// Top-k of the E=256 logits in lg (shared or global) with one warp; returns (in lane j < k)
+// the expert and weight of slot j.  Weights: exp(l_j - l_0) / sum over the kept logits.
+__device__ __forceinline__ void warp_topk256(const float* lg, int k, int lane, int& out_e, float& out_w) {
+    unsigned long long key[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) key[s] = topk_key(lg[lane + 32 * s], lane + 32 * s);
+    int my_e = -1;
+    float my_l = 0.f, l0 = 0.f;
+    for (int j = 0; j < k; ++j) {
+        unsigned long long best = 0;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) best = key[s] > best ? key[s] : best;
+        best = warp_max_u64(best);
+        const int e = 0xFFFF - (int)(best & 0xFFFFu);
+        const float l = lg[e];
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if ((e & 31) == lane && (e >> 5) == s) key[s] = 0;   // remove the winner
+        if (j == 0) l0 = (l != l) ? -INFINITY : l;
+        if (lane == j) { my_e = e; my_l = (l != l) ? -INFINITY : l; }
+    }
+    float ex = (lane < k) ? expf(my_l - l0) : 0.f;
+    float den = ex;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) den += __shfl_xor_sync(0xffffffffu, den, m);
+    out_e = my_e;
+    out_w = ex / den;
+}
+
+// Thread-block clusters: rank in the cluster, the split cluster barrier, and a 32-bit load
+// from the same offset in another CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ float ld_dsmem_f32(const void* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// Hand-off into another CTA of the cluster: a 32-bit store to its shared memory and a release
+// arrive on its mbarrier (same offsets as the local objects), and the matching acquire test.
+__device__ __forceinline__ void st_dsmem_u32(void* local, uint32_t rank, uint32_t v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote_release(uint64_t* local_bar, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_bar)), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+__device__ __forceinline__ bool mbar_test_wait_acq_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// GPU-scope release add / acquire load on a global counter.
+__device__ __forceinline__ void red_release_add(unsigned int* p, unsigned int v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// Warp-level bf16 MMA m16n8k16 with fp32 accumulation (operands in registers).  Used by the
+// one-token GEMV as a dot-product unit: every column of B holds the same activations, so
+// every column of D holds the 16 row dots.
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Warm L2 with [p, p + bytes) split over the threads of a grid (each thread up to 4 KB pieces).
 __device__ __forceinline__ void prefetch_l2_range(const uint8_t* p, size_t bytes, size_t worker, size_t nworkers) {
     for (size_t o = worker * 4096; o < bytes; o += nworkers * 4096) {
@@ -402,6 +531,30 @@ cudaError_t launch_down(const FfnArgs& a, cudaStream_t st, unsigned long long* l
 cudaError_t launch_combine(int T, int d, const float* acc, uint16_t* y, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_decode_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_decode_down(const FfnArgs& a, uint16_t* y, cudaStream_t st, unsigned long long* launches);
+// One-token forward in one launch (route + gate/up + down + combine).  Returns
+// cudaErrorNotSupported, with nothing launched, when the shape or the GPU does not fit it.
+struct FusedDecodeArgs {
+    int d, E, k, I;
+    const uint16_t* x;
+    const uint16_t* w_router;
+    const float* bias;
+    const uint8_t* w_routed;   // packed buffers (header first)
+    const uint8_t* w_shared;
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm;
+    int32_t* pos;
+    int32_t* tiles;
+    int32_t* num_tiles;
+    int* status;               // status word and counters (64 ints)
+    unsigned long long* logit_words;   // [8][E]: (call tag << 32) | fp32 logit bits, one copy per cluster rank; no other kernel writes it
+    float* acc;                // fp32 [d], zero between calls: the weighted sum
+    uint16_t* y;
+    unsigned long long* trace; // tuning builds (MOE_TRACE) only
+};
+cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_pack(int E, int N, int K, const moe_q4& m, int pair_slot, int pair_count, uint8_t* dst,
                         const int* mode, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_scale_check(size_t n, const uint16_t* scales, int* mode, cudaStream_t st,

@@ -27,54 +27,6 @@ namespace moe {
 namespace {
 
 
-// Order-preserving key: larger logit first, then lower expert index.  NaN counts as -inf
-// and -0 as +0 (they compare equal to +0).
-__device__ __forceinline__ unsigned long long topk_key(float v, int e) {
-    if (v != v) v = -INFINITY;
-    if (v == 0.0f) v = 0.0f;
-    uint32_t u = __float_as_uint(v);
-    uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return ((unsigned long long)o << 32) | (uint32_t)(0xFFFFu - (uint32_t)e);
-}
-
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-        unsigned long long o = __shfl_xor_sync(0xffffffffu, v, m);
-        v = o > v ? o : v;
-    }
-    return v;
-}
-
-// Top-k of the E=256 logits in lg (shared or global) with one warp; returns (in lane j < k)
-// the expert and weight of slot j.  Weights: exp(l_j - l_0) / sum over the kept logits.
-__device__ __forceinline__ void warp_topk256(const float* lg, int k, int lane, int& out_e, float& out_w) {
-    unsigned long long key[8];
-#pragma unroll
-    for (int s = 0; s < 8; ++s) key[s] = topk_key(lg[lane + 32 * s], lane + 32 * s);
-    int my_e = -1;
-    float my_l = 0.f, l0 = 0.f;
-    for (int j = 0; j < k; ++j) {
-        unsigned long long best = 0;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) best = key[s] > best ? key[s] : best;
-        best = warp_max_u64(best);
-        const int e = 0xFFFF - (int)(best & 0xFFFFu);
-        const float l = lg[e];
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-            if ((e & 31) == lane && (e >> 5) == s) key[s] = 0;   // remove the winner
-        if (j == 0) l0 = (l != l) ? -INFINITY : l;
-        if (lane == j) { my_e = e; my_l = (l != l) ? -INFINITY : l; }
-    }
-    float ex = (lane < k) ? expf(my_l - l0) : 0.f;
-    float den = ex;
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) den += __shfl_xor_sync(0xffffffffu, den, m);
-    out_e = my_e;
-    out_w = ex / den;
-}
-
 // ---------------------------------------------------------------------------------------
 // Exact logit of (token row xrow, expert row wrow) in the fixed order, computed by one warp:
 // lane l is partial sum l (columns 256*i + 8*l + j, i ascending, j = 0..7, fmaf from 0); the

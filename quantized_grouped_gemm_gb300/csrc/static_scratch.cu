@@ -4,8 +4,8 @@
 // output device pointers from a host program that owns every allocation, or a service loop
 // that must not allocate once it has started.  moe_forward_decode_static serves them: its
 // scratch (status word and counters, router logits, gate/up accumulators, the fp32 output sum)
-// is a fixed array in this file's device memory.  It runs the same three decode kernels as
-// moe_forward with T = 1.
+// is a fixed array in this file's device memory.  It runs the same kernels as moe_forward with
+// T = 1 (the fused one-launch kernel when it fits, else the three decode kernels).
 //
 // The array is shared by every call on a device and keeps the previous call's contents; each
 // call clears the part that must start at zero (status word and counters) with an async memset
@@ -40,13 +40,16 @@ uint8_t* scratch_address(int dev) {
     return g_scratch_ptr[dev];
 }
 
-// Scratch layout inside the array: status + counters, fp32 sum [d], logits [8][E] + g/u [k+1][2][I].
+// Scratch layout inside the array: status + counters, fp32 sum [d], logits [8][E] followed by
+// g/u [k+1][2][I] (GEMV kernels) or the per-unit partial outputs (fused kernel), then the
+// fused kernel's tagged logits.
 WsLayout static_layout(const moe_shape& s) {
     WsLayout L{};
     size_t o = 0;
     L.status = o; o = align_up(o + 64 * 4, 256);
     L.acc = o; o = align_up(o + (size_t)s.d * 4, 256);
     L.dec = o; o = align_up(o + (size_t)kDecodeMaxT * s.E * 4 + (size_t)(s.k + 1) * 2 * s.I * 4, 256);
+    L.fzlog = o; o = align_up(o + (size_t)8 * s.E * 8, 256);
     L.total = o;
     L.nblk = 1;
     return L;
@@ -80,8 +83,31 @@ extern "C" int moe_forward_decode_static(const moe_shape* s, const uint16_t* x, 
     uint8_t* ws = scratch_address(dev);
     if (!ws) return MOE_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // status word and every counter must start at zero
-    if (cudaMemsetAsync(ws + L.status, 0, 64 * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+    // status word and every counter must start at zero; word 4 (the fused kernel's epoch of its
+    // tagged logits) must not go back to an earlier value, so it is left alone
+    if (cudaMemsetAsync(ws + L.status, 0, 4 * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(ws + L.status + 5 * 4, 0, 59 * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+    // and the fp32 sum (zero after every completed call; cleared here all the same)
+    if (cudaMemsetAsync(ws + L.acc, 0, (size_t)s->d * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+    {   // one launch for the whole token when it fits (as moe_forward)
+        FusedDecodeArgs fa{};
+        fa.d = s->d; fa.E = s->E; fa.k = s->k; fa.I = s->I;
+        fa.x = x; fa.w_router = w_router; fa.bias = logit_bias;
+        fa.w_routed = static_cast<const uint8_t*>(packed_routed);
+        fa.w_shared = static_cast<const uint8_t*>(packed_shared);
+        fa.topk_idx = rt->topk_idx_dev; fa.topk_w = rt->topk_w_dev; fa.counts = rt->counts_dev;
+        fa.offsets = rt->offsets_dev; fa.perm = rt->perm_dev; fa.pos = rt->pos_dev; fa.tiles = rt->tiles_dev;
+        fa.num_tiles = rt->num_tiles_dev;
+        fa.status = reinterpret_cast<int*>(ws + L.status);
+        fa.logit_words = reinterpret_cast<unsigned long long*>(ws + L.fzlog);
+        fa.acc = reinterpret_cast<float*>(ws + L.acc);
+        fa.y = y;
+        unsigned long long nf = 0;
+        const cudaError_t ef = launch_decode_fused(fa, st, &nf);
+        count_launches(nf);
+        if (ef != cudaErrorNotSupported) return ef == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
 
     RouteArgs ra{};
     ra.T = 1; ra.d = s->d; ra.E = s->E; ra.k = s->k; ra.I = s->I; ra.tile_rows = 32;

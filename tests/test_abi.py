@@ -80,3 +80,30 @@ def test_argument_validation_without_gpu(lib):
     assert lib.moe_route(ctypes.byref(z), None, None, None, None, None, 0, None, None) == _lib.MOE_OK
     assert lib.moe_error_string(_lib.MOE_ERR_WORKSPACE).decode() != "unknown error"
     assert lib.moe_launch_count() == 0
+
+
+def _static_scratch_limit():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return int(re.search(r"#define MOE_STATIC_SCRATCH_BYTES (\d+)", src).group(1))
+
+
+def _static_scratch_needed(d, I, E=256, k=8):
+    """Bytes the no-workspace decode call needs, as its header documents (each part rounded up
+    to 256): status words, fp32 sum [d], decode scratch, tagged router logits."""
+    up = lambda v: (v + 255) // 256 * 256
+    return up(256) + up(d * 4) + up(8 * E * 4 + (k + 1) * 2 * I * 4) + up(8 * E * 8)
+
+
+def test_static_scratch_rejects_what_does_not_fit(lib):
+    """Rejected on the host before any CUDA call (the pointers are never dereferenced)."""
+    big = _lib.moe_shape(1, 7168, 256, 8, 8192, 8192, 64)
+    # guard: only call with dummy pointers when the shape is certain to be refused
+    assert _static_scratch_needed(7168, 8192) > _static_scratch_limit()
+    assert _static_scratch_needed(2048, 512) <= _static_scratch_limit()   # the decode workload fits
+    rt = _lib.moe_routing(*([256] * 8))
+    fake = ctypes.c_void_p(1 << 20)   # 256-byte aligned, never used
+    rc = lib.moe_forward_decode_static(ctypes.byref(big), fake, fake, None, fake, fake, ctypes.byref(rt), fake, None)
+    assert rc == _lib.MOE_ERR_WORKSPACE
+    two = _lib.moe_shape(2, 1024, 256, 8, 256, 256, 64)
+    rc = lib.moe_forward_decode_static(ctypes.byref(two), fake, fake, None, fake, fake, ctypes.byref(rt), fake, None)
+    assert rc == _lib.MOE_ERR_UNSUPPORTED

@@ -45,19 +45,3 @@ def test_static_scratch_decode_matches_workspace_forward_two_calls():
         ref = oracle.route(x, lay.w_router)
         out = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared)
         assert_output_close(y_to_f64(y_st), out, f"static-scratch call {call} vs oracle")
-
-
-def test_static_scratch_rejects_what_does_not_fit():
-    L = moe.lib()
-    rt = moe.Routing(1)
-    big = moe.shape(1, 7168, I=8192)          # scratch > MOE_STATIC_SCRATCH_BYTES
-    z = torch.zeros(16, dtype=torch.int16, device="cuda")
-    rc = L.moe_forward_decode_static(ctypes.byref(big), ctypes.c_void_p(z.data_ptr()), ctypes.c_void_p(z.data_ptr()),
-                                     None, ctypes.c_void_p(z.data_ptr()), ctypes.c_void_p(z.data_ptr()), rt.ref(),
-                                     ctypes.c_void_p(z.data_ptr()), None)
-    assert rc == moe.MOE_ERR_WORKSPACE
-    two = moe.shape(2, 1024, I=256)
-    rc = L.moe_forward_decode_static(ctypes.byref(two), ctypes.c_void_p(z.data_ptr()), ctypes.c_void_p(z.data_ptr()),
-                                     None, ctypes.c_void_p(z.data_ptr()), ctypes.c_void_p(z.data_ptr()), rt.ref(),
-                                     ctypes.c_void_p(z.data_ptr()), None)
-    assert rc == moe.MOE_ERR_UNSUPPORTED
