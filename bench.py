@@ -288,7 +288,7 @@ def run_ours(args, rank, world, local):
         bytes_layer = sh.E * sh.d * 2 + 9 * (3 * sh.d * sh.I // 2 + 3 * sh.d * sh.I // 64 * 4)
         gbs = bytes_layer / (us_tok_layer * 1e-6) / 1e9
         res["roofline"] = dict(bound="hbm", achieved=gbs, peak=P["hbm_gbs"], unit="GB/s", frac=gbs / P["hbm_gbs"],
-                               traffic=None, kernel="whole decode layer (route + gate/up GEMV + down GEMV)",
+                               traffic=None, kernel="decode_fused (one launch per layer: route + gate/up + down + combine)",
                                bytes_per_token_layer=bytes_layer, peak_source=P["source"])
         res["config"] = dict(workload=wl.name, T=1, d=sh.d, E=sh.E, k=sh.k, I=sh.I, I_shared=sh.I_shared,
                              layers=layers, l2="inputs larger than L2: 40 layer copies of the weights, 18 GB",

@@ -231,18 +231,85 @@ __global__ void __launch_bounds__(192, 1)
 // are recomputed.  The result equals top-8 over all 256 exact logits.
 // Also writes the block's per-expert counts.
 // ---------------------------------------------------------------------------------------
+// Exact logits (fixed order, as warp_pinned_logit) of two experts for the token row held in
+// registers, with both rows' loads issued before the arithmetic.
+template <int NI>
+__device__ __forceinline__ void warp_pinned_logit2(const uint4 (&xv)[8], const uint16_t* w0, const uint16_t* w1,
+                                                   int lane, float& l0, float& l1) {
+    uint4 a[NI], b[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        a[i] = ld_nc_v4(w0 + 256 * i + 8 * lane);
+        b[i] = ld_nc_v4(w1 + 256 * i + 8 * lane);
+    }
+    float p = 0.f, q = 0.f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        p = fmaf(bf16lo(xv[i].x), bf16lo(a[i].x), p);  q = fmaf(bf16lo(xv[i].x), bf16lo(b[i].x), q);
+        p = fmaf(bf16hi(xv[i].x), bf16hi(a[i].x), p);  q = fmaf(bf16hi(xv[i].x), bf16hi(b[i].x), q);
+        p = fmaf(bf16lo(xv[i].y), bf16lo(a[i].y), p);  q = fmaf(bf16lo(xv[i].y), bf16lo(b[i].y), q);
+        p = fmaf(bf16hi(xv[i].y), bf16hi(a[i].y), p);  q = fmaf(bf16hi(xv[i].y), bf16hi(b[i].y), q);
+        p = fmaf(bf16lo(xv[i].z), bf16lo(a[i].z), p);  q = fmaf(bf16lo(xv[i].z), bf16lo(b[i].z), q);
+        p = fmaf(bf16hi(xv[i].z), bf16hi(a[i].z), p);  q = fmaf(bf16hi(xv[i].z), bf16hi(b[i].z), q);
+        p = fmaf(bf16lo(xv[i].w), bf16lo(a[i].w), p);  q = fmaf(bf16lo(xv[i].w), bf16lo(b[i].w), q);
+        p = fmaf(bf16hi(xv[i].w), bf16hi(a[i].w), p);  q = fmaf(bf16hi(xv[i].w), bf16hi(b[i].w), q);
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        p = p + __shfl_xor_sync(0xffffffffu, p, m);
+        q = q + __shfl_xor_sync(0xffffffffu, q, m);
+    }
+    l0 = p;
+    l1 = q;
+}
+
+__device__ __forceinline__ void pinned_logit_pair(const uint4 (&xv)[8], const uint16_t* xrow, const uint16_t* w_router,
+                                                  int d, int e0, int e1, int lane, float& l0, float& l1) {
+    const uint16_t* w0 = w_router + (size_t)e0 * d;
+    const uint16_t* w1 = w_router + (size_t)e1 * d;
+    switch (d / 256) {
+        case 1: warp_pinned_logit2<1>(xv, w0, w1, lane, l0, l1); return;
+        case 2: warp_pinned_logit2<2>(xv, w0, w1, lane, l0, l1); return;
+        case 4: warp_pinned_logit2<4>(xv, w0, w1, lane, l0, l1); return;
+        case 8: warp_pinned_logit2<8>(xv, w0, w1, lane, l0, l1); return;
+        default:
+            l0 = warp_pinned_logit(xrow, w0, d, lane, nullptr);
+            l1 = warp_pinned_logit(xrow, w1, d, lane, nullptr);
+    }
+}
+
+// Order key of a logit (NaN as -inf, -0 as +0); larger key = larger logit, never 0.
+__device__ __forceinline__ uint32_t logit_key32(float f) {
+    if (f != f) f = -INFINITY;
+    if (f == 0.0f) f = 0.0f;
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key32_logit(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// ---------------------------------------------------------------------------------------
+// route_certify_topk: one warp per token, 16 tokens per CTA (two CTAs per 32-token block).
+// From the tensor-core partial logits l~ and the bound delta of each expert it keeps the
+// candidates l~ + delta >= lo with lo = (8th largest l~) - max delta (at least eight experts
+// have an exact logit >= lo, so no other expert can be in the exact top-8), recomputes their
+// exact logits in the fixed order, two at a time, and takes the top-k among them.  More than
+// 32 candidates: all 256 are recomputed.  Per-block expert counts are added for the scan.
+// ---------------------------------------------------------------------------------------
+constexpr int kCertTokens = 16;
+
 __global__ void __launch_bounds__(512) route_certify_topk(RouteArgs a, int KS) {
     __shared__ uint32_t s_mask[256];
-    __shared__ float s_all[16][256];
+    __shared__ float s_all[kCertTokens][256];
+    __shared__ int s_cand[kCertTokens][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t0 = blockIdx.x * kRouteBlockTokens;
+    const int tok = blockIdx.x * kCertTokens + warp;
     const float* part = reinterpret_cast<const float*>(a.ws + a.L.rpart);
     const float* wnorm = reinterpret_cast<const float*>(a.ws + a.L.wnorm);
     const float c = 2.0f * (float)(a.d + 4 + 35) * 1.1920928955078125e-7f;   // 2^-23
     if (threadIdx.x < 256) s_mask[threadIdx.x] = 0;
     __syncthreads();
-    for (int rep = 0; rep < 2; ++rep) {          // warp w: tokens w and w + 16 of the block
-    const int tl = warp + 16 * rep, tok = t0 + tl;
     if (tok < a.T) {
         const uint16_t* xrow = a.x + (size_t)tok * a.d;
         // the token row in registers (first 8 column groups) and ||x_t||
@@ -252,6 +319,14 @@ __global__ void __launch_bounds__(512) route_certify_topk(RouteArgs a, int KS) {
         for (int i = 0; i < 8; ++i) {
             xv[i] = make_uint4(0, 0, 0, 0);
             if (i < a.d / 256) xv[i] = ld_nc_v4(xrow + 256 * i + 8 * lane);
+        }
+        float lt[8], dl[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int e = lane + 32 * s;
+            float v = 0.f;
+            for (int q = 0; q < KS; ++q) v += part[((size_t)q * a.T + tok) * 256 + e];
+            lt[s] = v;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -270,75 +345,73 @@ __global__ void __launch_bounds__(512) route_certify_topk(RouteArgs a, int KS) {
 #pragma unroll
         for (int m = 16; m >= 1; m >>= 1) nx += __shfl_xor_sync(0xffffffffu, nx, m);
         nx = sqrtf(nx);
-        // approximate logits and their error bounds; lane holds experts lane + 32 s
-        float lt[8], dl[8];
+        float dmax = 0.f;
+        uint32_t key[8];
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
             const int e = lane + 32 * s;
-            float v = 0.f;
-            for (int q = 0; q < KS; ++q) v += part[((size_t)q * a.T + tok) * 256 + e];
             const float b = a.bias ? a.bias[e] : 0.f;
-            v += b;
-            lt[s] = v;
-            dl[s] = c * nx * wnorm[e] + 4.7683716e-7f * (fabsf(v) + fabsf(b) + 1.0f);   // + 2^-21 (|l|+|b|+1)
+            lt[s] += b;
+            dl[s] = c * nx * wnorm[e] + 4.7683716e-7f * (fabsf(lt[s]) + fabsf(b) + 1.0f);   // + 2^-21 (|l|+|b|+1)
+            dmax = fmaxf(dmax, dl[s]);
+            key[s] = logit_key32(lt[s]);
         }
-        // lo = min over the 8 largest approximate logits of (l~ - delta)
-        unsigned long long key[8];
-#pragma unroll
-        for (int s = 0; s < 8; ++s) key[s] = topk_key(lt[s], lane + 32 * s);
-        float lo = INFINITY;
+        dmax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(dmax)));   // dmax >= 0
+        // the 8th largest l~: eight rounds, each removing one holder of the largest key
+        uint32_t top = 0;
         for (int j = 0; j < 8; ++j) {
-            unsigned long long best = 0;
+            uint32_t mx = key[0];
 #pragma unroll
-            for (int s = 0; s < 8; ++s) best = key[s] > best ? key[s] : best;
-            best = warp_max_u64(best);
-            const int e = 0xFFFF - (int)(best & 0xFFFFu);
-            float v = 0.f;
+            for (int s = 1; s < 8; ++s) mx = max(mx, key[s]);
+            top = __reduce_max_sync(0xffffffffu, mx);
+            int mine = 0x7fffffff;
+#pragma unroll
+            for (int s = 7; s >= 0; --s)
+                if (key[s] == top) mine = 32 * s + lane;
+            const int who = __reduce_min_sync(0xffffffffu, mine);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                if ((e & 31) == lane && (e >> 5) == s) { key[s] = 0; v = lt[s] - dl[s]; }
-            v = __shfl_sync(0xffffffffu, v, e & 31);
-            lo = fminf(lo, v);
+                if (32 * s + lane == who) key[s] = 0u;
         }
-        // candidates, as one 256-bit mask held across the warp (word s in every lane)
+        const float lo = __fsub_rd(key32_logit(top), dmax);
         uint32_t cm[8];
         int ncand = 0;
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-            const bool cand = !(lt[s] + dl[s] < lo);      // NaN-safe: NaN stays a candidate
+            const bool cand = !(__fadd_ru(lt[s], dl[s]) < lo);      // NaN-safe: NaN stays a candidate
             cm[s] = __ballot_sync(0xffffffffu, cand);
             ncand += __popc(cm[s]);
         }
         int e_out;
         float w_out;
         if (ncand <= 32) {
-            int my_e = -1;
-            float my_l = -INFINITY;
-            int j = 0;
+            // candidate j (ascending expert) goes to lane j
+            int before = 0;
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
-                uint32_t m = cm[s];
-                while (m) {
-                    const int b = __ffs(m) - 1;
-                    m &= m - 1;
-                    const int e = b + 32 * s;
-                    const float l = pinned_logit_any(xv, xrow, a.w_router + (size_t)e * a.d, a.d, lane,
-                                                     a.bias ? a.bias + e : nullptr);
-                    if (lane == j) { my_e = e; my_l = l; }
-                    ++j;
-                }
+                if (cm[s] >> lane & 1u) s_cand[warp][before + __popc(cm[s] & ((1u << lane) - 1u))] = lane + 32 * s;
+                before += __popc(cm[s]);
             }
-            // top-k among the (<= 32) exact candidate logits, one per lane
-            unsigned long long k1 = my_e >= 0 ? topk_key(my_l, my_e) : 0ull;
+            __syncwarp();
+            int my_e = -1;
+            float my_l = -INFINITY;
+            for (int j0 = 0; j0 < ncand; j0 += 2) {
+                const int e0 = s_cand[warp][j0], e1 = j0 + 1 < ncand ? s_cand[warp][j0 + 1] : e0;
+                float l0, l1;
+                pinned_logit_pair(xv, xrow, a.w_router, a.d, e0, e1, lane, l0, l1);
+                if (a.bias) { l0 = l0 + a.bias[e0]; l1 = l1 + a.bias[e1]; }
+                if (lane == j0) { my_e = e0; my_l = l0; }
+                if (lane == j0 + 1) { my_e = e1; my_l = l1; }
+            }
+            // top-k among the exact candidate logits, one per lane
+            uint32_t k1 = my_e >= 0 ? logit_key32(my_l) : 0u;
             int sel_e = -1;
             float sel_l = 0.f, l0 = 0.f;
             for (int jj = 0; jj < a.k; ++jj) {
-                const unsigned long long best = warp_max_u64(k1);
-                const int e = 0xFFFF - (int)(best & 0xFFFFu);
-                const int src = __ffs(__ballot_sync(0xffffffffu, my_e == e)) - 1;
-                const float l = __shfl_sync(0xffffffffu, my_l, src);
-                if (my_e == e) k1 = 0;
-                const float lc = (l != l) ? -INFINITY : l;
+                const uint32_t best = __reduce_max_sync(0xffffffffu, k1);
+                const int e = __reduce_min_sync(0xffffffffu, (k1 == best && my_e >= 0) ? my_e : 0x7fffffff);
+                if (my_e == e) k1 = 0u;
+                const float lc = key32_logit(best);
                 if (jj == 0) l0 = lc;
                 if (lane == jj) { sel_e = e; sel_l = lc; }
             }
@@ -349,10 +422,12 @@ __global__ void __launch_bounds__(512) route_certify_topk(RouteArgs a, int KS) {
             e_out = sel_e;
             w_out = ex / den;
         } else {
-            for (int e = 0; e < 256; ++e) {
-                const float l = pinned_logit_any(xv, xrow, a.w_router + (size_t)e * a.d, a.d, lane,
-                                                 a.bias ? a.bias + e : nullptr);
-                if (lane == (e & 31)) s_all[warp][e] = l;
+            for (int e = 0; e < 256; e += 2) {
+                float l0, l1;
+                pinned_logit_pair(xv, xrow, a.w_router, a.d, e, e + 1, lane, l0, l1);
+                if (a.bias) { l0 = l0 + a.bias[e]; l1 = l1 + a.bias[e + 1]; }
+                if (lane == (e & 31)) s_all[warp][e] = l0;
+                if (lane == ((e + 1) & 31)) s_all[warp][e + 1] = l1;
             }
             __syncwarp();
             warp_topk256(s_all[warp], a.k, lane, e_out, w_out);
@@ -360,14 +435,14 @@ __global__ void __launch_bounds__(512) route_certify_topk(RouteArgs a, int KS) {
         if (lane < a.k) {
             a.topk_idx[(size_t)tok * a.k + lane] = e_out;
             a.topk_w[(size_t)tok * a.k + lane] = w_out;
-            atomicOr(&s_mask[e_out], 1u << tl);
+            atomicOr(&s_mask[e_out], 1u << warp);
         }
-    }
+        __syncwarp();
     }
     __syncthreads();
-    if (threadIdx.x < 256) {
+    if (threadIdx.x < 256 && s_mask[threadIdx.x]) {   // per 32-token block counts (cleared by the scan)
         int32_t* blk_counts = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
-        blk_counts[(size_t)blockIdx.x * 256 + threadIdx.x] = __popc(s_mask[threadIdx.x]);
+        atomicAdd(&blk_counts[(size_t)(blockIdx.x / 2) * 256 + threadIdx.x], __popc(s_mask[threadIdx.x]));
     }
 }
 
@@ -440,9 +515,18 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) c[u] = blk_counts[(size_t)(b + u) * E + e];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) { blk_base[(size_t)(b + u) * E + e] = r; r += c[u]; }
+            for (int u = 0; u < 8; ++u) {
+                blk_base[(size_t)(b + u) * E + e] = r;
+                r += c[u];
+                blk_counts[(size_t)(b + u) * E + e] = 0;   // the next call adds into zeros
+            }
         }
-        for (; b < b1; ++b) { const int c = blk_counts[(size_t)b * E + e]; blk_base[(size_t)b * E + e] = r; r += c; }
+        for (; b < b1; ++b) {
+            const int c = blk_counts[(size_t)b * E + e];
+            blk_base[(size_t)b * E + e] = r;
+            r += c;
+            blk_counts[(size_t)b * E + e] = 0;
+        }
     }
     if (part != 0) return;          // warps 8..31 are done; the rest uses named barrier 1 (256 threads)
     const int off = s_off[e];
@@ -701,7 +785,7 @@ cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned l
     if (err != cudaSuccess) return err;
     router_wnorm<<<256 / 4, 128, 0, st>>>(a);
     router_tc<<<dim3((a.T + 127) / 128, KS), 192, kRtSmem, st>>>(tm_x, tm_w, a, KS);
-    route_certify_topk<<<nblk, 512, 0, st>>>(a, KS);
+    route_certify_topk<<<(a.T + kCertTokens - 1) / kCertTokens, 512, 0, st>>>(a, KS);
     route_scan<<<1, 1024, 0, st>>>(a);
     route_scatter<<<dim3(nblk, a.k), 256, 0, st>>>(a);
     *launches += 5;
