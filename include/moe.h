@@ -170,7 +170,9 @@ int moe_ffn_down(const moe_shape* shape, const moe_routing* routing, const void*
                  const void* packed_shared_dev, void* workspace_dev, size_t workspace_bytes,
                  const moe_options* options, void* stream);
 
-/* Step a10: y [T][d] bf16 (round to nearest even) from the fp32 token-order sum. */
+/* Step a10: y [T][d] bf16 (round to nearest even) from the fp32 token-order sum, which it then
+ * clears: moe_grouped_ffn adds into a sum that a fresh (zeroed) workspace or the previous
+ * moe_combine / moe_forward left at zero. */
 int moe_combine(const moe_shape* shape, const moe_routing* routing, void* workspace_dev, size_t workspace_bytes,
                 uint16_t* y_dev, const moe_options* options, void* stream);
 

@@ -618,22 +618,26 @@ __global__ void __launch_bounds__(256) route_scatter(RouteArgs a) {
         s_pos[tl] = p;
     }
     __syncthreads();
-    // gather this slot's rows into expert order: xs[p] = x[t]
+    // gather this slot's rows into expert order: xs[p] = x[t]; a warp per row, eight 16-byte
+    // loads in flight per lane before the stores
     uint16_t* xs = reinterpret_cast<uint16_t*>(a.ws + a.L.xs);
-    const int cpr = a.d / 8;                       // 16-byte chunks per row
-    const int total = ntok * cpr;
-    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-        const int r = idx / cpr, c = idx % cpr;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int r = warp; r < ntok; r += blockDim.x / 32) {
         const int p = s_pos[r];
         if (p < 0) continue;
-        const uint4 v = ld_nc_v4(a.x + (size_t)(t0 + r) * a.d + 8 * c);
-        *reinterpret_cast<uint4*>(xs + (size_t)p * a.d + 8 * c) = v;
+        const uint16_t* src = a.x + (size_t)(t0 + r) * a.d;
+        uint16_t* dst = xs + (size_t)p * a.d;
+        for (int c0 = 8 * lane; c0 < a.d; c0 += 8 * 32 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c0 + 256 * u < a.d) v[u] = ld_nc_v4(src + c0 + 256 * u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c0 + 256 * u < a.d) *reinterpret_cast<uint4*>(dst + c0 + 256 * u) = v[u];
+        }
     }
-    // clear this CTA's share of the fp32 token-order sum of the block
-    float4* acc = reinterpret_cast<float4*>(a.ws + a.L.acc) + (size_t)t0 * (a.d / 4);
-    const int n4 = ntok * (a.d / 4);
-    for (int idx = slot * blockDim.x + threadIdx.x; idx < n4; idx += k * blockDim.x)
-        acc[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // (the fp32 token-order sum is zero here: a fresh workspace is, and moe_combine clears it)
 }
 
 // ---------------------------------------------------------------------------------------
