@@ -257,8 +257,13 @@ int moe_ffn_gate_up(const moe_shape* s, const uint16_t* x, const moe_routing* rt
     if (rc != MOE_OK) return rc == 1 ? MOE_OK : rc;
     FfnArgs a = ffn_args(s, x, rt, wr, wsh, ws);
     unsigned long long n = 0;
-    cudaError_t e = is_decode(s, op) ? launch_decode_gate_up(a, static_cast<cudaStream_t>(stream), &n)
-                                     : launch_gate_up(a, static_cast<cudaStream_t>(stream), &n);
+    cudaError_t e;
+    if (is_decode(s, op)) {
+        e = launch_decode_gate_up(a, static_cast<cudaStream_t>(stream), &n);
+    } else {   // tiles of more than kSmallRows token rows on tensor cores, the rest on warp MMA
+        e = launch_gate_up(a, static_cast<cudaStream_t>(stream), &n);
+        if (e == cudaSuccess) e = launch_gate_up_small(a, static_cast<cudaStream_t>(stream), &n);
+    }
     g_launches += n;
     return cuda_status(e);
 }
@@ -275,6 +280,7 @@ int moe_ffn_down(const moe_shape* s, const moe_routing* rt, const void* wr, cons
         e = launch_decode_down(a, nullptr, static_cast<cudaStream_t>(stream), &n);
     } else {
         e = launch_down(a, static_cast<cudaStream_t>(stream), &n);
+        if (e == cudaSuccess) e = launch_down_small(a, static_cast<cudaStream_t>(stream), &n);
     }
     g_launches += n;
     return cuda_status(e);

@@ -470,7 +470,7 @@ __device__ __forceinline__ int block_exclusive_scan256(int v, int* s_tmp) {
 
 __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     __shared__ int s_tmp[8];
-    __shared__ int s_tot[4];
+    __shared__ int s_tot[4];   // [0] block-map tiles, [1] large GEMM blocks, [2] small GEMM blocks
     __shared__ int s_part[4][256];
     __shared__ int s_off[256];
     const int E = 256;
@@ -548,16 +548,31 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     // run at the same time share the block's activation rows in L2).  The shared expert
     // (expert index E) comes first and covers token rows 0..T-1.
     const int MTgu = a.I / kTileRows, MTdn = a.d / 256;   // 128 gate+up row pairs; 256-row down tiles
-    const int nn = (run + kMaxN - 1) / kMaxN;
-    const int nsh = (a.T + kMaxN - 1) / kMaxN;
+    // experts with at most kSmallRows rows go to the small-tile lists as one block
+    const bool small = run > 0 && run <= kSmallRows;
+    const int nn = small ? 0 : (run + kMaxN - 1) / kMaxN;
+    // the shared expert runs in kSmallRows-row blocks on the warp-MMA kernel when the chunk is
+    // small enough that the routed groups mostly are (T <= 1024: 8T/E <= 32 rows on average)
+    const bool sh_small = a.T <= 1024;
+    const int nsh = sh_small ? 0 : (a.T + kMaxN - 1) / kMaxN;
+    const int nshs = sh_small ? (a.T + kSmallRows - 1) / kSmallRows : 0;
     const int nbase = block_exclusive_scan256(nn, s_tmp);
     if (e == E - 1) s_tot[1] = nbase + nn;
     named_bar_sync(1, 256);
+    const int sbase = block_exclusive_scan256(small ? 1 : 0, s_tmp);
+    if (e == E - 1) s_tot[2] = sbase + (small ? 1 : 0);
+    named_bar_sync(1, 256);
     int4* gu = reinterpret_cast<int4*>(a.ws + a.L.gu_tiles);
     int4* dn = reinterpret_cast<int4*>(a.ws + a.L.dn_tiles);
+    int4* gus = reinterpret_cast<int4*>(a.ws + a.L.gu_small);
+    int4* dns = reinterpret_cast<int4*>(a.ws + a.L.dn_small);
     auto emit = [&](int slot, int ex, int r0, int rows) {
         for (int m = 0; m < MTgu; ++m) gu[(size_t)slot * MTgu + m] = make_int4(ex, r0, rows, m);
         for (int m = 0; m < MTdn; ++m) dn[(size_t)slot * MTdn + m] = make_int4(ex, r0, rows, m);
+    };
+    auto emit_small = [&](int slot, int ex, int r0, int rows) {
+        for (int m = 0; m < MTgu; ++m) gus[(size_t)slot * MTgu + m] = make_int4(ex, r0, rows, m);
+        for (int m = 0; m < MTdn; ++m) dns[(size_t)slot * MTdn + m] = make_int4(ex, r0, rows, m);
     };
     if (nn > 0) {
         const int base_rows = run / nn, rem = run % nn;
@@ -568,16 +583,20 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
             r0 += rows;
         }
     }
+    if (small) emit_small(nshs + sbase, e, off, run);
     for (int i = e; i < nsh; i += E) {   // shared expert token blocks
         const int base_rows = a.T / nsh, rem = a.T % nsh;
         const int r0 = i * base_rows + min(i, rem);
         emit(i, E, r0, base_rows + (i < rem ? 1 : 0));
     }
+    for (int i = e; i < nshs; i += E) emit_small(i, E, i * kSmallRows, min(kSmallRows, a.T - i * kSmallRows));
     if (e == 0) {
         *a.num_tiles = s_tot[0];
-        const int total_n = nsh + s_tot[1];
+        const int total_n = nsh + s_tot[1], total_s = nshs + s_tot[2];
         *reinterpret_cast<int32_t*>(a.ws + a.L.gu_num) = total_n * MTgu;
         *reinterpret_cast<int32_t*>(a.ws + a.L.dn_num) = total_n * MTdn;
+        *reinterpret_cast<int32_t*>(a.ws + a.L.gu_small_num) = total_s * MTgu;
+        *reinterpret_cast<int32_t*>(a.ws + a.L.dn_small_num) = total_s * MTdn;
     }
 }
 
