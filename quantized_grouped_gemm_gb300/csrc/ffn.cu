@@ -36,6 +36,8 @@ constexpr int kWRows = 256;                        // MMA N: weight rows of a ti
 constexpr int kActBytes = kTokRows * 128;          // 128 rows x 64 bf16 (one K block)
 constexpr int kWdqBytes = kWRows * 128;            // 256 rows x 64 bf16
 constexpr int kRawBytes = kChunkPairBytes;         // 9216
+constexpr int kEpiRows = kEpiWarps * 32;           // token rows of the epilogue (one per thread)
+constexpr int kStageStride = 64 * 4 + 16;          // 64 fp32 + 16 bytes of padding (bank spread)
 
 #ifndef MOE_GU_RAW
 #define MOE_GU_RAW 4
@@ -50,7 +52,7 @@ constexpr int kRawBytes = kChunkPairBytes;         // 9216
 #define MOE_DN_RAW 3
 #endif
 #ifndef MOE_DN_WDQ
-#define MOE_DN_WDQ 4
+#define MOE_DN_WDQ 3
 #endif
 #ifndef MOE_DN_ACT
 #define MOE_DN_ACT 4
@@ -64,7 +66,10 @@ struct Cfg {
     static constexpr int act_off = 0;
     static constexpr int wdq_off = act_off + ACT * kActBytes;
     static constexpr int raw_off = wdq_off + WDQ * kWdqBytes;
-    static constexpr int bar_off = raw_off + RAW * kRawBytes;
+    // down: epilogue staging of 64 output columns per token row (row stride 272 bytes)
+    static constexpr int stage_off = raw_off + RAW * kRawBytes;
+    static constexpr int stage_bytes = kDown ? kEpiRows * kStageStride : 0;
+    static constexpr int bar_off = stage_off + stage_bytes;
 };
 
 struct Bars {
@@ -169,6 +174,17 @@ __device__ __forceinline__ void dequant_store4(uint4 codes, uint32_t s2, uint32_
                      : "memory");
     }
 }
+
+// Bulk add of `bytes` fp32 from shared memory into global memory (TMA reduction; 16-byte
+// aligned addresses, bytes % 16 == 0); completion tracked per thread by bulk groups.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return (uint32_t)f32_to_bf16_rn(a) | ((uint32_t)f32_to_bf16_rn(b) << 16);
@@ -382,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                // 256 columns of d starting at 256*wt: acc[token][n] += w * y
+                // 256 columns of d starting at 256*wt: acc[token][n] += w * y, 64 columns at a time
+                // through the thread's staging row and one bulk reduce-add (TMA) per piece
                 int tk = 0;
                 float w = 0.f;
                 if (live) {
@@ -396,16 +413,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 float* ap = p.acc + (size_t)tk * p.d + (size_t)wt * kWRows;
-                for (int c = 0; c < 16; ++c) {
-                    uint32_t Y[16];
-                    tmem_ld16(taddr + 16 * c, Y);
-                    tmem_ld_wait();
-                    if (live) {
+                uint8_t* srow = smem + C::stage_off + (32 * q + lane) * kStageStride;
+                for (int pc = 0; pc < 4; ++pc) {
+                    bulk_wait_read0();   // the previous piece has left the staging row
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            atomicAdd(reinterpret_cast<float4*>(ap + 16 * c + 4 * v),
-                                      make_float4(w * __uint_as_float(Y[4 * v]), w * __uint_as_float(Y[4 * v + 1]),
-                                                  w * __uint_as_float(Y[4 * v + 2]), w * __uint_as_float(Y[4 * v + 3])));
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t Y[16];
+                        tmem_ld16(taddr + 64 * pc + 16 * c, Y);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const uint32_t a = smem_u32(srow + 64 * c + 16 * v);
+                            asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a),
+                                         "f"(w * __uint_as_float(Y[4 * v])), "f"(w * __uint_as_float(Y[4 * v + 1])),
+                                         "f"(w * __uint_as_float(Y[4 * v + 2])), "f"(w * __uint_as_float(Y[4 * v + 3]))
+                                         : "memory");
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    if (live) {
+                        bulk_reduce_add_f32(ap + 64 * pc, srow, 256);
+                        bulk_commit();
                     }
                 }
             }
@@ -416,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             use[buf]++;
         }
         if (!ok && lane == 0) raise_abort(abort, p.status);
+        if (kDown) bulk_wait0();   // every bulk reduce-add of this thread has completed
     }
 
     tc_fence_before();
