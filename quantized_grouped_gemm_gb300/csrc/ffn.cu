@@ -480,7 +480,9 @@ FfnParams make_params(const FfnArgs& a, bool gate_up) {
     p.perm = a.perm;
     p.topk_w = a.topk_w;
     p.status = reinterpret_cast<int*>(a.ws + a.L.status);
-    p.trace = reinterpret_cast<unsigned long long*>(a.ws + a.L.dec);
+#ifdef MOE_TRACE
+    p.trace = reinterpret_cast<unsigned long long*>(a.ws + a.L.trace);
+#endif
     p.T = a.T; p.d = a.d; p.I = a.I; p.E = a.E; p.k = a.k;
     return p;
 }
