@@ -5,13 +5,14 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ou
 A step is one pass of the whole hot path (route -> grouped FFN -> combine) over one batch of
 synthetic input of the workload.  Default workload: the 512-token prefill chunk (T=512, d=2048,
 256 experts, top-8, I=512 + shared expert), whose 455 MB of 4-bit weights exceed L2, so every
-step streams its inputs from HBM.  Timing: W untimed steps, then K steps between CUDA events on
+step streams its inputs from HBM (a workload whose layer fits in L2 rotates through enough
+independent layer copies to exceed it).  Timing: W untimed steps, then K steps between CUDA events on
 the launching stream (each step is replayed from CUDA graphs of the library calls), barrier +
 synchronize on both sides, max over ranks.  Multi-GPU (torchrun): every rank runs its own
 chunks (weak scaling, no collective on the data path).
 
---impl reference times the CPU oracle (the reference of this build) on bounded samples of the
-same workload on the host cores.
+--impl reference times the CPU oracle on bounded samples of the same workload on the host
+cores.
 """
 from __future__ import annotations
 
@@ -140,13 +141,18 @@ def run_ours(args, rank, world, local):
     sh = wl.shape
     decode = sh.T == 1
     T = wl.chunk or sh.T
-    layers = wl.layers if decode else 1
     shp = moe.shape(T, sh.d, sh.E, sh.k, sh.I, sh.I_shared)
+    L2_BYTES = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 10**6)
+    # 4-bit codes plus a bf16 scale and bias per 64 weights, gate/up/down of every expert
+    layer_bytes = sum(n * (3 * sh.d * i // 2 + 3 * sh.d * i // 16) for n, i in ((sh.E, sh.I), (1, sh.I_shared)))
+    # a step's weights must not sit in L2 between steps: a workload whose layer fits rotates
+    # through enough independent layer copies to exceed twice the L2 size
+    layers = wl.layers if decode else max(1, -(-2 * L2_BYTES // layer_bytes))
 
     def to_dev(a):
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a)).to(dev)
 
-    # weights: one layer (prefill) or `layers` independent copies (decode)
+    # weights: `layers` independent copies (decode; small prefill layers), else one layer
     L = []
     for li in range(layers):
         lay = configs.make_layer(wl, layer=li)
@@ -192,44 +198,54 @@ def run_ours(args, rank, world, local):
                                     stream)
             graphs["step"] = g
         else:
-            l0 = L[0]
-            calls = {
-                "route": lambda: moe.moe_route(shp, x_in, l0["wr"], l0["bias"], rt, ws, opts, stream),
-                "gate_up": lambda: moe.moe_ffn_gate_up(shp, x_in, rt, l0["pr"], l0["ps"], ws, opts, stream),
-                "down": lambda: moe.moe_ffn_down(shp, rt, l0["pr"], l0["ps"], ws, opts, stream),
-                "combine": lambda: moe.moe_combine(shp, rt, ws, y, opts, stream),
-            }
-            x_in.copy_(xs[0])
-            for f in calls.values():
-                f()
-            stream.synchronize()
-            n0 = moe.moe_launch_count()
-            for name, f in calls.items():
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
+            # one set of phase graphs per (layer copy, resident chunk buffer): a step reads its
+            # chunk in place; step s runs layer s % layers on chunk s % chunks
+            def calls_for(lw, xc):
+                return {
+                    "route": lambda: moe.moe_route(shp, xc, lw["wr"], lw["bias"], rt, ws, opts, stream),
+                    "gate_up": lambda: moe.moe_ffn_gate_up(shp, xc, rt, lw["pr"], lw["ps"], ws, opts, stream),
+                    "down": lambda: moe.moe_ffn_down(shp, rt, lw["pr"], lw["ps"], ws, opts, stream),
+                    "combine": lambda: moe.moe_combine(shp, rt, ws, y, opts, stream),
+                }
+            nsets = int(np.lcm(layers, len(xs)))
+            for gi in range(nsets):
+                for f in calls_for(L[gi % layers], xs[gi % len(xs)]).values():
                     f()
-                graphs[name] = g
-    launches_per_step = moe.moe_launch_count() - n0
+            stream.synchronize()
+            graphs = []
+            for gi in range(nsets):
+                if gi == 0:
+                    n0 = moe.moe_launch_count()
+                gc = {}
+                for name, f in calls_for(L[gi % layers], xs[gi % len(xs)]).items():
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        f()
+                    gc[name] = g
+                graphs.append(gc)
+                if gi == 0:
+                    launches_one_chunk = moe.moe_launch_count() - n0
+    launches_per_step = moe.moe_launch_count() - n0 if decode else launches_one_chunk
     torch.cuda.synchronize()
 
-    # per-chunk inputs: prefill graphs read x_in; a step copies its chunk into x_in first
-    # (device-to-device, T*d*2 bytes) -- part of the step for both the graph and eager paths
+    # prefill: a step runs the graphs of its chunk, which read the chunk where it resides;
+    # decode: a step copies its token's activations (4 KB) into the graph's input buffer first
     def step(s, ev=None):
         if decode:
             x_in.copy_(x_all[s % nsteps_x:s % nsteps_x + 1], non_blocking=True)
             graphs["step"].replay()
         else:
-            x_in.copy_(xs[s % len(xs)], non_blocking=True)
-            graphs["route"].replay()
+            gc = graphs[s % len(graphs)]
+            gc["route"].replay()
             if ev is not None:
                 ev[0].record(stream)
-            graphs["gate_up"].replay()
+            gc["gate_up"].replay()
             if ev is not None:
                 ev[1].record(stream)
-            graphs["down"].replay()
+            gc["down"].replay()
             if ev is not None:
                 ev[2].record(stream)
-            graphs["combine"].replay()
+            gc["combine"].replay()
 
     dist = None
     if world > 1:
@@ -291,7 +307,8 @@ def run_ours(args, rank, world, local):
                                traffic=None, kernel="decode_fused (one launch per layer: route + gate/up + down + combine)",
                                bytes_per_token_layer=bytes_layer, peak_source=P["source"])
         res["config"] = dict(workload=wl.name, T=1, d=sh.d, E=sh.E, k=sh.k, I=sh.I, I_shared=sh.I_shared,
-                             layers=layers, l2="inputs larger than L2: 40 layer copies of the weights, 18 GB",
+                             layers=layers, l2=f"inputs larger than L2: {layers} layer copies of the weights, "
+                                                 f"{layers * layer_bytes / 1e9:.0f} GB",
                              parallelism=f"replicas x{world}")
     else:
         value = world * T * K / (ms_total / 1000.0)
@@ -318,18 +335,20 @@ def run_ours(args, rank, world, local):
                           ffn_weight_gbs=A["weights_bytes"] / (ffn_ms * 1e-3) / 1e9,
                           experts_touched=A["touched"], other_ms=ms_step - ffn_ms)
         res["config"] = dict(workload=wl.name, T=T, d=sh.d, E=sh.E, k=sh.k, I=sh.I, I_shared=sh.I_shared,
-                             chunks=sh.T // T, l2="inputs larger than L2: 455 MB of 4-bit weights per step",
+                             chunks=sh.T // T, layers=layers,
+                             l2=f"inputs larger than L2: {layers} layer cop{'y' if layers == 1 else 'ies'} of "
+                                f"{layer_bytes / 1e6:.0f} MB of 4-bit weights, a step reads one",
                              parallelism=f"replicas x{world}")
 
     # ---- end to end through the public API with host buffers (pinned), copies timed
     if not decode:
         xh = [t.cpu().pin_memory() for t in xs[:4]]
         yh = torch.empty(T, sh.d, dtype=torch.int16).pin_memory()
-        l0 = L[0]
         with torch.cuda.stream(stream):
             def e2e_step(s):
+                lw = L[s % layers]
                 x_in.copy_(xh[s % len(xh)], non_blocking=True)
-                moe.moe_forward(shp, x_in, l0["wr"], l0["bias"], l0["pr"], l0["ps"], rt, ws, y, opts, stream)
+                moe.moe_forward(shp, x_in, lw["wr"], lw["bias"], lw["pr"], lw["ps"], rt, ws, y, opts, stream)
                 yh.copy_(y, non_blocking=True)
             for s in range(3):
                 e2e_step(s)
@@ -405,7 +424,9 @@ def run_reference(args, rank, world):
     from moe_workload import configs
     wl = configs.WORKLOADS[args.workload]
     K = args.steps if args.steps is not None else 10
-    n = 4 if wl.shape.T != 1 else 8
+    # the same 32-token sample as the in-line CPU baseline, smaller when many steps are asked
+    # for, so that the whole run stays within a few minutes
+    n = 8 if wl.shape.T == 1 else int(min(32, max(4, 4 * (240 // (K + args.warmup)))))
     smp = OracleSampler(wl)
     for s in range(args.warmup):
         smp.run(n, seed=100 + s)
