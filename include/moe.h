@@ -10,10 +10,12 @@
  *   grouped_ffn  per expert group: SwiGLU FFN whose 4-bit group-affine weights are rebuilt
  *                in bf16 tile by tile on chip (64 weights share one bf16 scale and bias,
  *                w = scale*q + bias), fp32 accumulation; the output projection is weighted by
- *                the routing score and summed with the always-on shared expert in fp32
- *                (sections "Dequantize weights during matrix multiplication" and "Reduce
- *                intermediate and state traffic").
- *   combine      the fp32 token-order sum is written out as bf16.
+ *                the routing score (1 for the always-on shared expert) in fp32 (sections
+ *                "Dequantize weights during matrix multiplication" and "Reduce intermediate
+ *                and state traffic").
+ *   combine      each token's k weighted routed rows and its shared row are summed in fp32
+ *                (a fixed order: routing slot 0..k-1, then the shared expert) and written
+ *                out as bf16.
  * Batch-1 decode (T <= options.decode_max_tokens) runs the same calls on GEMV kernels
  * (section "Optimize the single-row weight path").
  *
@@ -121,7 +123,8 @@ int moe_check_shape(const moe_shape* shape);
 
 /* Bytes of the caller-provided workspace for this shape (0 if the shape is unsupported).
  * The workspace holds routing scratch, the gathered rows, the intermediate h, the fp32
- * token-order sum and the device status word.  One workspace serves one stream at a time. */
+ * weighted output rows ((k+1) T x d), the fp32 token-order sum of the decode kernels and the
+ * device status word.  One workspace serves one stream at a time. */
 size_t moe_workspace_bytes(const moe_shape* shape, const moe_options* options);
 
 /* Number of int32 triples the block map (moe_routing.tiles) can need: ceil(k*T/tile_rows) + E. */
@@ -143,7 +146,7 @@ int moe_pack_weights(const moe_shape* shape, const moe_expert_weights* src, int 
 /* Step a1-a6: router logits (x [T][d] bf16, w_router [E][d] bf16, optional fp32 logit_bias
  * [E] added after the dot product), top-k with weights, histogram, prefix scan, stable
  * scatter, block map.  Also gathers the routed rows into expert order inside the workspace
- * for moe_grouped_ffn and clears the fp32 token-order sum.
+ * for moe_grouped_ffn.
  * The logit of (t, e) is fixed bit-exactly: 32 partial fp32 sums, sum l taking
  * k = 256*i + 8*l + j (i ascending, j = 0..7) with fused multiply-adds from 0, then the
  * tree s[i] += s[i+m] for m = 16, 8, 4, 2, 1, then + logit_bias[e]. */
@@ -152,11 +155,13 @@ int moe_route(const moe_shape* shape, const uint16_t* x_dev, const uint16_t* w_r
               size_t workspace_bytes, const moe_options* options, void* stream);
 
 /* Steps a7-a9: for every expert group and the shared expert, gate/up projections with
- * SwiGLU (h kept to 16 bits as a bf16 pair), output projection, and the fp32 weighted
- * accumulation into the token-order sum held in the workspace (routing weight topk_w for
- * routed rows, 1 for the shared expert).  Weights are the packed stacks written by
- * moe_pack_weights (routed: E experts with I; shared: 1 expert with I_shared).
- * Requires moe_route on the same workspace and stream first. */
+ * SwiGLU (h kept to 16 bits as a bf16 pair), output projection, and the fp32 weighting
+ * (routing weight topk_w for routed rows, 1 for the shared expert).  Prefill writes every
+ * weighted output row into the workspace (rows in expert-group order, then the shared
+ * expert's rows); decode shapes (T <= options.decode_max_tokens) add into the fp32 token-order
+ * sum instead.  Weights are the packed stacks written by moe_pack_weights (routed: E experts
+ * with I; shared: 1 expert with I_shared).  Requires moe_route on the same workspace and
+ * stream first. */
 int moe_grouped_ffn(const moe_shape* shape, const uint16_t* x_dev, const moe_routing* routing,
                     const void* packed_routed_dev, const void* packed_shared_dev, void* workspace_dev,
                     size_t workspace_bytes, const moe_options* options, void* stream);
@@ -170,8 +175,10 @@ int moe_ffn_down(const moe_shape* shape, const moe_routing* routing, const void*
                  const void* packed_shared_dev, void* workspace_dev, size_t workspace_bytes,
                  const moe_options* options, void* stream);
 
-/* Step a10: y [T][d] bf16 (round to nearest even) from the fp32 token-order sum, which it then
- * clears: moe_grouped_ffn adds into a sum that a fresh (zeroed) workspace or the previous
+/* Step a10: y [T][d] bf16 (round to nearest even).  Prefill: the sum, in fp32 and in a fixed
+ * order, of each token's k weighted routed rows (found through routing.pos) and its shared
+ * row, as moe_grouped_ffn left them.  Decode shapes: the fp32 token-order sum, which it then
+ * clears: the decode kernels add into a sum that a fresh (zeroed) workspace or the previous
  * moe_combine / moe_forward left at zero. */
 int moe_combine(const moe_shape* shape, const moe_routing* routing, void* workspace_dev, size_t workspace_bytes,
                 uint16_t* y_dev, const moe_options* options, void* stream);

@@ -33,7 +33,7 @@ static EncodeTiledFn encode_fn() {
 }
 
 cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                              uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows) {
+                              uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
     EncodeTiledFn f = encode_fn();
     if (!f) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {cols, rows};
@@ -41,7 +41,8 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows,
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = f(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -261,8 +262,12 @@ int moe_ffn_gate_up(const moe_shape* s, const uint16_t* x, const moe_routing* rt
     if (is_decode(s, op)) {
         e = launch_decode_gate_up(a, static_cast<cudaStream_t>(stream), &n);
     } else {   // tiles of more than kSmallRows token rows on tensor cores, the rest on warp MMA
+#if MOE_FFN_TMEM
+        e = launch_gate_up_tm(a, static_cast<cudaStream_t>(stream), &n);
+#else
         e = launch_gate_up(a, static_cast<cudaStream_t>(stream), &n);
         if (e == cudaSuccess) e = launch_gate_up_small(a, static_cast<cudaStream_t>(stream), &n);
+#endif
     }
     g_launches += n;
     return cuda_status(e);
@@ -279,8 +284,12 @@ int moe_ffn_down(const moe_shape* s, const moe_routing* rt, const void* wr, cons
     if (is_decode(s, op)) {
         e = launch_decode_down(a, nullptr, static_cast<cudaStream_t>(stream), &n);
     } else {
+#if MOE_FFN_TMEM
+        e = launch_down_tm(a, static_cast<cudaStream_t>(stream), &n);
+#else
         e = launch_down(a, static_cast<cudaStream_t>(stream), &n);
         if (e == cudaSuccess) e = launch_down_small(a, static_cast<cudaStream_t>(stream), &n);
+#endif
     }
     g_launches += n;
     return cuda_status(e);
@@ -300,13 +309,21 @@ int moe_combine(const moe_shape* s, const moe_routing* rt, void* ws, size_t ws_b
     Opts op;
     if ((rc = get_opts(o, &op)) != MOE_OK) return rc;
     if (s->T == 0) return MOE_OK;
-    (void)rt;
     if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
     if (!y || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(*s);
+    uint8_t* w8 = static_cast<uint8_t*>(ws);
     unsigned long long n = 0;
-    cudaError_t e = launch_combine(s->T, s->d, reinterpret_cast<const float*>(static_cast<uint8_t*>(ws) + L.acc), y,
-                                   static_cast<cudaStream_t>(stream), &n);
+    cudaError_t e;
+    if (MOE_FFN_TMEM && !is_decode(s, op) && ffn_rows_output(s->T, s->d, s->k)) {
+        // prefill: the down projection left weighted rows in Y; sum each token's rows
+        if ((rc = check_routing(rt)) != MOE_OK) return rc;
+        e = launch_combine_rows(s->T, s->d, s->k, reinterpret_cast<const float*>(w8 + L.Y), rt->pos_dev, y,
+                                static_cast<cudaStream_t>(stream), &n);
+    } else {
+        e = launch_combine(s->T, s->d, reinterpret_cast<const float*>(w8 + L.acc), y, static_cast<cudaStream_t>(stream),
+                           &n);
+    }
     g_launches += n;
     return cuda_status(e);
 }

@@ -15,8 +15,11 @@
 // Two persistent CTAs per SM, each 8 compute warps + 1 producer warp.  A unit is a tile of the
 // small list: (expert, first row, rows <= 32, weight tile).  The producer streams, per K block
 // of 64, the packed chunk pair (one 9216-byte bulk copy) and the activation rows of the block
-// (a 32-row TMA tile with 128-byte swizzle; for the down projection the hi and lo halves of
-// h) into a ring of shared-memory slots.
+// (for the down projection the hi and lo halves of h) into a ring of shared-memory slots.  An
+// activation block is two unswizzled 32-row x 32-column TMA boxes with 64-byte rows: the eight
+// lanes of a quarter warp then read two whole rows, 128 contiguous bytes, with no bank
+// conflict (a 64-column box in 128-byte swizzle puts rows 2p and 2p+1 of a quarter warp on the
+// same banks).
 //   gate/up: warp w owns i-rows 16w .. 16w+15 of the 128-row tile for both gate and up, so g
 //            and u of the same (i, token) meet in one thread: h = silu(g) * u is written as a
 //            bf16 hi/lo pair.
@@ -33,7 +36,8 @@ namespace {
 constexpr int kSmWarps = 8;                          // compute warps
 constexpr int kSmThreads = (kSmWarps + 1) * 32;      // + producer warp
 constexpr int kSmTok = kSmallRows;                   // token rows of an activation tile (TMA box)
-constexpr int kSmActBytes = kSmTok * 128;            // 32 rows x 64 bf16
+constexpr int kSmActBytes = kSmTok * 128;            // 32 rows x 64 bf16: two 32-column boxes
+constexpr int kSmHalfBytes = kSmActBytes / 2;        // one box, rows of 64 bytes
 constexpr int kSmRingGU = 4, kSmRingDN = 3;   // per CTA; two CTAs per SM
 
 template <bool kDown>
@@ -67,10 +71,16 @@ struct SmParams {
 __device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 __device__ __forceinline__ uint32_t lds16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
 
-// Activation fragment of token row n of a 32 x 64 tile in 128-byte swizzle: columns
-// 8t..8t+7 (c4 = 0) or 32+8t..32+8t+7 (c4 = 1) as 8 bf16.
+// Activation fragment of token row n of a 32 x 64 block: columns 8t..8t+7 (c4 = 0, first box)
+// or 32+8t..32+8t+7 (c4 = 1, second box) as 8 bf16.
 __device__ __forceinline__ uint4 act_frag(const uint8_t* tile, int n, int t, int c4) {
-    return *reinterpret_cast<const uint4*>(tile + n * 128 + (((4 * c4 + t) ^ (n & 7)) << 4));
+    return *reinterpret_cast<const uint4*>(tile + c4 * kSmHalfBytes + n * 64 + 16 * t);
+}
+
+// One activation block: columns x0 .. x0+63 of rows y0 .. y0+31 as two 32-column boxes.
+__device__ __forceinline__ void load_act_block(uint8_t* dst, const CUtensorMap* tm, int x0, int y0, uint64_t* bar) {
+    tma_load_2d(dst, tm, x0, y0, bar);
+    tma_load_2d(dst + kSmHalfBytes, tm, x0 + 32, y0, bar);
 }
 
 // Dequantised A fragments of rows r0 = rb + g and r1 = r0 + 8 of one 128-row chunk: v[0..3]
@@ -263,10 +273,10 @@ __global__ void __launch_bounds__(kSmThreads, 2)
                     uint8_t* at = aring + s * C::ACTS * kSmActBytes;
                     if (kDown) {
                         const int hrow0 = e < p.E ? row0 : p.k * p.T + row0;
-                        tma_load_2d(at, &tm_a, kb * kBK, hrow0, &full[s]);
-                        tma_load_2d(at + kSmActBytes, &tm_a, p.I + kb * kBK, hrow0, &full[s]);
+                        load_act_block(at, &tm_a, kb * kBK, hrow0, &full[s]);
+                        load_act_block(at + kSmActBytes, &tm_a, p.I + kb * kBK, hrow0, &full[s]);
                     } else {
-                        tma_load_2d(at, e < p.E ? &tm_a : &tm_b, kb * kBK, row0, &full[s]);
+                        load_act_block(at, e < p.E ? &tm_a : &tm_b, kb * kBK, row0, &full[s]);
                     }
                 }
             }
@@ -339,9 +349,9 @@ cudaError_t launch_gate_up_small(const FfnArgs& a, cudaStream_t st, unsigned lon
     cudaError_t err = set_small_smem_attr<false>();
     if (err != cudaSuccess) return err;
     CUtensorMap tm_xs, tm_x;
-    err = make_tmap_bf16_2d(&tm_xs, a.ws + a.L.xs, (uint64_t)a.k * a.T, a.d, (uint64_t)a.d * 2, kBK, kSmTok);
+    err = make_tmap_bf16_2d(&tm_xs, a.ws + a.L.xs, (uint64_t)a.k * a.T, a.d, (uint64_t)a.d * 2, 32, kSmTok, false);
     if (err != cudaSuccess) return err;
-    err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, kSmTok);
+    err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, 32, kSmTok, false);
     if (err != cudaSuccess) return err;
     ffn_small_kernel<false><<<2 * a.num_sms, kSmThreads, SmCfg<false>::smem, st>>>(tm_xs, tm_x, make_small_params(a, true));
     *launches += 1;
@@ -352,8 +362,8 @@ cudaError_t launch_down_small(const FfnArgs& a, cudaStream_t st, unsigned long l
     cudaError_t err = set_small_smem_attr<true>();
     if (err != cudaSuccess) return err;
     CUtensorMap tm_h;
-    err = make_tmap_bf16_2d(&tm_h, a.ws + a.L.H, (uint64_t)(a.k + 1) * a.T, 2 * (uint64_t)a.I, (uint64_t)a.I * 4, kBK,
-                            kSmTok);
+    err = make_tmap_bf16_2d(&tm_h, a.ws + a.L.H, (uint64_t)(a.k + 1) * a.T, 2 * (uint64_t)a.I, (uint64_t)a.I * 4, 32,
+                            kSmTok, false);
     if (err != cudaSuccess) return err;
     ffn_small_kernel<true><<<2 * a.num_sms, kSmThreads, SmCfg<true>::smem, st>>>(tm_h, tm_h, make_small_params(a, false));
     *launches += 1;

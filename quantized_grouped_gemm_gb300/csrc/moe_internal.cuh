@@ -62,7 +62,8 @@ struct WsLayout {
     size_t dn_small_num;
     size_t xs;          // bf16 [k*T][d] rows in expert-group order
     size_t H;           // bf16 [(k+1)*T][2*I] (hi | lo)
-    size_t acc;         // fp32 [T][d] token-order sum
+    size_t acc;         // fp32 [T][d] token-order sum (decode kernels)
+    size_t Y;           // fp32 [(k+1)T][d] weighted down-projection rows (prefill), row order of H
     size_t dec;         // decode scratch: logits fp32 [8][E], g/u fp32 [8][k+1][2][I]
     size_t fzlog;       // u64 [8][E]: tagged logits of the one-launch decode kernel (eight copies)
     size_t trace;       // tuning builds (MOE_TRACE): 64 KB of phase timestamps
@@ -72,10 +73,33 @@ struct WsLayout {
 
 constexpr int kRouteBlockTokens = 32;   // tokens per routing block (one warp, one bitmask)
 constexpr int kMaxN = 128;              // max token rows of a GEMM tile (MMA M)
+#ifndef MOE_FFN_TMEM
+#define MOE_FFN_TMEM 1                  // grouped FFN with the dequantised weights in TMEM (one tile list)
+#endif
+#ifndef MOE_GU_ROWS
+#define MOE_GU_ROWS 128                 // token rows of a gate/up block (TMEM-operand FFN)
+#endif
+#ifndef MOE_DN_ROWS
+#define MOE_DN_ROWS 128                 // token rows of a down-projection block (TMEM-operand FFN)
+#endif
 constexpr int kSmallRows = 32;          // token blocks up to this size run on the warp-MMA kernel
 constexpr int kDecodeMaxT = 8;          // largest T the decode (GEMV) kernels take
+// token rows of a gate/up and of a down-projection block (smaller blocks were measured slower
+// at 4096 tokens: per-token dequant and MMA issue outweigh the overlap they allow)
+constexpr int kGuRows = MOE_FFN_TMEM ? MOE_GU_ROWS : kMaxN;
+constexpr int kDnRows = MOE_FFN_TMEM ? MOE_DN_ROWS : kMaxN;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Prefill output path of the down projection.  When the weighted rows ((k+1) T x d fp32) fit
+// well inside L2 they are stored as rows and summed per token by combine_rows (plain stores, a
+// fixed summation order); larger chunks add into the fp32 token-order sum (T x d, L2-resident)
+// with bulk reduce-adds, which spares the round trip of the rows through HBM.
+#ifndef MOE_ROWS_OUT_MB
+#define MOE_ROWS_OUT_MB 64
+#endif
+constexpr size_t kRowsOutputMaxBytes = (size_t)MOE_ROWS_OUT_MB << 20;
+inline bool ffn_rows_output(int T, int d, int k) { return (size_t)(k + 1) * T * d * 4 <= kRowsOutputMaxBytes; }
 
 // K slices of the tensor-core router GEMM (partial sums, combined when picking candidates)
 inline int router_kslices(int d) { return d / 64 >= 16 ? 4 : (d / 64 >= 4 ? 2 : 1); }
@@ -95,10 +119,13 @@ inline WsLayout ws_layout(const moe_shape& s) {
     WsLayout L{};
     const int T = s.T, d = s.d, E = s.E, k = s.k, I = s.I;
     L.nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
-    const int shared_nt = (T + kMaxN - 1) / kMaxN;
-    const int routed_nt = gemm_ntile_bound(k * T, E);
+    const int shared_nt = (T + kGuRows - 1) / kGuRows;
+    const int routed_nt = k * T / kGuRows + E + 1;
     L.max_gu = (routed_nt + shared_nt) * (I / kTileRows);
-    L.max_dn = (routed_nt + shared_nt) * (d / 256);
+    // down blocks of at most kDnRows rows: at most rows/kDnRows + groups per expert set
+    const int shared_nd = (T + kDnRows - 1) / kDnRows;
+    const int routed_nd = k * T / kDnRows + E + 1;
+    L.max_dn = (routed_nd + shared_nd) * (d / 256);
     size_t o = 0;
     L.status = o; o = align_up(o + 64 * 4, 256);
     L.rpart = o; o = align_up(o + (size_t)router_kslices(d) * T * E * 4, 256);
@@ -118,6 +145,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
     L.xs = o; o = align_up(o + (size_t)k * T * d * 2 + 256 * d * 2, 1024);
     L.H = o; o = align_up(o + (size_t)(k + 1) * T * 2 * I * 2 + 256 * 2 * I * 2, 1024);
     L.acc = o; o = align_up(o + (size_t)T * d * 4, 256);
+    L.Y = o; o = align_up(o + (size_t)(k + 1) * T * d * 4, 256);
     L.dec = o; o = align_up(o + decode_scratch_bytes(d, E, k, I), 256);
     L.fzlog = o; o = align_up(o + (size_t)8 * E * 8, 256);
 #ifdef MOE_TRACE
@@ -312,6 +340,18 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// The same MMA with A (M x K, K-major: row m in lane m, K pairs packed per 32-bit column) read
+// from tensor memory at column a_tmem.
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -328,6 +368,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x 32 bits x 32 columns (one column per register) into TMEM.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ---------------------------- misc ---------------------------------------------------
 __device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
@@ -341,14 +394,25 @@ __device__ __forceinline__ float bf16f(uint16_t v) { return __uint_as_float((uin
 
 // Eight weights of one packed 32-bit word (pairs (0,1) (2,3) (4,5) (6,7) as bf16x2) with the
 // per-row scale and bias pairs s2 / b2 of the buffer's scale encoding.
+// Scaled-code encoding: a bf16 bit pattern n < 256 has the value n * 2^-133 (a subnormal, or a
+// number of the lowest normal binade), so the code at bits 0..3 of a half is read in place as
+// q * 2^-133 and the code at bits 4..7 as 16 q * 2^-133, the latter against the stored scale
+// divided by 16 (exact).  Both products are exactly q * scale, and the FMA rounds q * scale +
+// bias once: the same bf16 as with each code shifted down first.  Codes at bits 8..15 take
+// one shift of the word.
 template <bool kDenorm>
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&v)[4]) {
+    if (kDenorm) {
+        const uint32_t s16 = bf16x2_fma(s2, 0x3D803D80u, 0x80008000u);      // S * 2^-4 (+ -0)
+        const uint32_t w8 = w >> 8;
+        v[0] = bf16x2_fma(w & 0x000F000Fu, s2, b2);                         // q * 2^-133 * S + b
+        v[1] = bf16x2_fma(w & 0x00F000F0u, s16, b2);                        // 16 q * 2^-133 * S / 16 + b
+        v[2] = bf16x2_fma(w8 & 0x000F000Fu, s2, b2);
+        v[3] = bf16x2_fma(w8 & 0x00F000F0u, s16, b2);
+    } else {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const uint32_t c = (u == 0 ? w : (w >> (4 * u))) & 0x000F000Fu;
-        if (kDenorm) {
-            v[u] = bf16x2_fma(c, s2, b2);                                   // q * 2^-133 * S + b
-        } else {
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t c = (u == 0 ? w : (w >> (4 * u))) & 0x000F000Fu;
             const uint32_t q = bf16x2_fma(c | 0x43004300u, 0x3F803F80u, 0xC300C300u);   // (128 + q) - 128
             v[u] = bf16x2_fma(q, s2, b2);
         }
@@ -573,6 +637,10 @@ struct FusedDecodeArgs {
     uint16_t* y;
     unsigned long long* trace; // tuning builds (MOE_TRACE) only
 };
+cudaError_t launch_gate_up_tm(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_combine_rows(int T, int d, int k, const float* Y, const int32_t* pos, uint16_t* y, cudaStream_t st,
+                                unsigned long long* launches);
+cudaError_t launch_down_tm(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_pack(int E, int N, int K, const moe_q4& m, int pair_slot, int pair_count, uint8_t* dst,
                         const int* mode, cudaStream_t st, unsigned long long* launches);
@@ -581,6 +649,7 @@ cudaError_t launch_scale_check(size_t n, const uint16_t* scales, int* mode, cuda
 
 // Encodes 2-D bf16 tensor maps (host; driver entry point fetched through the runtime).
 cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                              uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
+                              uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
+                              bool swizzle128 = true);
 
 }  // namespace moe

@@ -543,21 +543,27 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     }
     if (e == E - 1) s_tot[0] = tbase + nt;
 
-    // GEMM tile lists: an expert's rows split into ceil(rows / kMaxN) near-equal token blocks;
-    // each block is repeated for every weight tile (weight tile innermost, so the CTAs that
-    // run at the same time share the block's activation rows in L2).  The shared expert
-    // (expert index E) comes first and covers token rows 0..T-1.
+    // GEMM tile lists: an expert's rows split into near-equal token blocks (gate/up: at most
+    // kGuRows rows; down: at most kDnRows); each block is repeated for every weight tile (weight
+    // tile innermost, so the CTAs that run at the same time share the block's activation rows
+    // in L2).  The shared expert (expert index E) comes first and covers token rows 0..T-1.
     const int MTgu = a.I / kTileRows, MTdn = a.d / 256;   // 128 gate+up row pairs; 256-row down tiles
     // experts with at most kSmallRows rows go to the small-tile lists as one block
-    const bool small = run > 0 && run <= kSmallRows;
-    const int nn = small ? 0 : (run + kMaxN - 1) / kMaxN;
+    // (the TMEM-operand FFN takes every block size from the main lists)
+    const bool small = !MOE_FFN_TMEM && run > 0 && run <= kSmallRows;
+    const int nn = small ? 0 : (run + kGuRows - 1) / kGuRows;
+    const int nd = small ? 0 : (run + kDnRows - 1) / kDnRows;
     // the shared expert runs in kSmallRows-row blocks on the warp-MMA kernel when the chunk is
     // small enough that the routed groups mostly are (T <= 1024: 8T/E <= 32 rows on average)
-    const bool sh_small = a.T <= 1024;
-    const int nsh = sh_small ? 0 : (a.T + kMaxN - 1) / kMaxN;
+    const bool sh_small = !MOE_FFN_TMEM && a.T <= 1024;
+    const int nsh = sh_small ? 0 : (a.T + kGuRows - 1) / kGuRows;
+    const int nshd = sh_small ? 0 : (a.T + kDnRows - 1) / kDnRows;
     const int nshs = sh_small ? (a.T + kSmallRows - 1) / kSmallRows : 0;
     const int nbase = block_exclusive_scan256(nn, s_tmp);
     if (e == E - 1) s_tot[1] = nbase + nn;
+    named_bar_sync(1, 256);
+    const int dbase = block_exclusive_scan256(nd, s_tmp);
+    if (e == E - 1) s_tot[3] = dbase + nd;
     named_bar_sync(1, 256);
     const int sbase = block_exclusive_scan256(small ? 1 : 0, s_tmp);
     if (e == E - 1) s_tot[2] = sbase + (small ? 1 : 0);
@@ -566,35 +572,37 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     int4* dn = reinterpret_cast<int4*>(a.ws + a.L.dn_tiles);
     int4* gus = reinterpret_cast<int4*>(a.ws + a.L.gu_small);
     int4* dns = reinterpret_cast<int4*>(a.ws + a.L.dn_small);
-    auto emit = [&](int slot, int ex, int r0, int rows) {
-        for (int m = 0; m < MTgu; ++m) gu[(size_t)slot * MTgu + m] = make_int4(ex, r0, rows, m);
-        for (int m = 0; m < MTdn; ++m) dn[(size_t)slot * MTdn + m] = make_int4(ex, r0, rows, m);
+    // nb near-equal blocks of `rows` rows from r0; block i goes to list slot base + i
+    auto split = [&](int4* list, int mt, int base, int ex, int r0, int rows, int nb) {
+        const int q = rows / nb, rem = rows % nb;
+        for (int i = 0; i < nb; ++i) {
+            const int n = q + (i < rem ? 1 : 0);
+            for (int m = 0; m < mt; ++m) list[(size_t)(base + i) * mt + m] = make_int4(ex, r0, n, m);
+            r0 += n;
+        }
     };
     auto emit_small = [&](int slot, int ex, int r0, int rows) {
         for (int m = 0; m < MTgu; ++m) gus[(size_t)slot * MTgu + m] = make_int4(ex, r0, rows, m);
         for (int m = 0; m < MTdn; ++m) dns[(size_t)slot * MTdn + m] = make_int4(ex, r0, rows, m);
     };
-    if (nn > 0) {
-        const int base_rows = run / nn, rem = run % nn;
-        int r0 = off;
-        for (int i = 0; i < nn; ++i) {
-            const int rows = base_rows + (i < rem ? 1 : 0);
-            emit(nsh + nbase + i, e, r0, rows);
-            r0 += rows;
-        }
-    }
+    if (nn > 0) split(gu, MTgu, nsh + nbase, e, off, run, nn);
+    if (nd > 0) split(dn, MTdn, nshd + dbase, e, off, run, nd);
     if (small) emit_small(nshs + sbase, e, off, run);
-    for (int i = e; i < nsh; i += E) {   // shared expert token blocks
-        const int base_rows = a.T / nsh, rem = a.T % nsh;
-        const int r0 = i * base_rows + min(i, rem);
-        emit(i, E, r0, base_rows + (i < rem ? 1 : 0));
+    // shared expert token blocks (one thread each)
+    for (int i = e; i < nsh; i += E) {
+        const int q = a.T / nsh, rem = a.T % nsh;
+        split(gu, MTgu, i, E, i * q + min(i, rem), q + (i < rem ? 1 : 0), 1);
+    }
+    for (int i = e; i < nshd; i += E) {
+        const int q = a.T / nshd, rem = a.T % nshd;
+        split(dn, MTdn, i, E, i * q + min(i, rem), q + (i < rem ? 1 : 0), 1);
     }
     for (int i = e; i < nshs; i += E) emit_small(i, E, i * kSmallRows, min(kSmallRows, a.T - i * kSmallRows));
     if (e == 0) {
         *a.num_tiles = s_tot[0];
-        const int total_n = nsh + s_tot[1], total_s = nshs + s_tot[2];
-        *reinterpret_cast<int32_t*>(a.ws + a.L.gu_num) = total_n * MTgu;
-        *reinterpret_cast<int32_t*>(a.ws + a.L.dn_num) = total_n * MTdn;
+        const int total_s = nshs + s_tot[2];
+        *reinterpret_cast<int32_t*>(a.ws + a.L.gu_num) = (nsh + s_tot[1]) * MTgu;
+        *reinterpret_cast<int32_t*>(a.ws + a.L.dn_num) = (nshd + s_tot[3]) * MTdn;
         *reinterpret_cast<int32_t*>(a.ws + a.L.gu_small_num) = total_s * MTgu;
         *reinterpret_cast<int32_t*>(a.ws + a.L.dn_small_num) = total_s * MTdn;
     }
