@@ -326,8 +326,7 @@ def run_ours(args, rank, world, local):
         else:
             ach = A["gu_flops"] / (gu_ms * 1e-3) / 1e12
             roof = dict(bound="tensor", achieved=ach, peak=P["bf16_tflops"], unit="TFLOP/s", frac=ach / P["bf16_tflops"])
-        roof.update(traffic=None, kernel="gate/up phase: ffn_kernel<0> (tcgen05, expert groups > 32 rows) + "
-                    "ffn_small_kernel<0> (warp MMA, groups <= 32 rows)", algorithmic_bytes=A["gu_bytes"],
+        roof.update(traffic=None, kernel="ffn_tm_kernel<0> (gate/up + SwiGLU; tcgen05, dequantised weights in TMEM)", algorithmic_bytes=A["gu_bytes"],
                     algorithmic_flops=A["gu_flops"], kernel_ms=gu_ms, peak_source=P["source"])
         res["roofline"] = roof
         ffn_ms = gu_ms + dn_ms

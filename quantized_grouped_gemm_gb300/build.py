@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["api.cu", "route.cu", "ffn.cu", "ffn_small.cu", "ffn_tm.cu", "decode.cu", "decode_fused.cu", "pack.cu", "static_scratch.cu"]
+SOURCES = ["api.cu", "route.cu", "ffn.cu", "decode.cu", "decode_fused.cu", "pack.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

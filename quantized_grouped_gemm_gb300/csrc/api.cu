@@ -261,13 +261,8 @@ int moe_ffn_gate_up(const moe_shape* s, const uint16_t* x, const moe_routing* rt
     cudaError_t e;
     if (is_decode(s, op)) {
         e = launch_decode_gate_up(a, static_cast<cudaStream_t>(stream), &n);
-    } else {   // tiles of more than kSmallRows token rows on tensor cores, the rest on warp MMA
-#if MOE_FFN_TMEM
+    } else {
         e = launch_gate_up_tm(a, static_cast<cudaStream_t>(stream), &n);
-#else
-        e = launch_gate_up(a, static_cast<cudaStream_t>(stream), &n);
-        if (e == cudaSuccess) e = launch_gate_up_small(a, static_cast<cudaStream_t>(stream), &n);
-#endif
     }
     g_launches += n;
     return cuda_status(e);
@@ -284,12 +279,7 @@ int moe_ffn_down(const moe_shape* s, const moe_routing* rt, const void* wr, cons
     if (is_decode(s, op)) {
         e = launch_decode_down(a, nullptr, static_cast<cudaStream_t>(stream), &n);
     } else {
-#if MOE_FFN_TMEM
         e = launch_down_tm(a, static_cast<cudaStream_t>(stream), &n);
-#else
-        e = launch_down(a, static_cast<cudaStream_t>(stream), &n);
-        if (e == cudaSuccess) e = launch_down_small(a, static_cast<cudaStream_t>(stream), &n);
-#endif
     }
     g_launches += n;
     return cuda_status(e);
@@ -315,7 +305,7 @@ int moe_combine(const moe_shape* s, const moe_routing* rt, void* ws, size_t ws_b
     uint8_t* w8 = static_cast<uint8_t*>(ws);
     unsigned long long n = 0;
     cudaError_t e;
-    if (MOE_FFN_TMEM && !is_decode(s, op) && ffn_rows_output(s->T, s->d, s->k)) {
+    if (!is_decode(s, op) && ffn_rows_output(s->T, s->d, s->k)) {
         // prefill: the down projection left weighted rows in Y; sum each token's rows
         if ((rc = check_routing(rt)) != MOE_OK) return rc;
         e = launch_combine_rows(s->T, s->d, s->k, reinterpret_cast<const float*>(w8 + L.Y), rt->pos_dev, y,

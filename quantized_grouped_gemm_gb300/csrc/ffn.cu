@@ -1,109 +1,108 @@
-// ffn.cu -- grouped SwiGLU FFN over packed 4-bit group-affine weights, sm_103a tcgen05.
+// ffn.cu -- grouped SwiGLU FFN over packed 4-bit group-affine weights, sm_103a tcgen05 with
+// the dequantised weights as the MMA's A operand in tensor memory.
 //
 // "Optimizing on-device inference for Apple Silicon" (Perplexity, 2026), section "Dequantize
 // weights during matrix multiplication": the grouped GEMM rebuilds one small bf16 weight tile
-// at a time in on-chip memory, multiplies it with the routed activation rows, accumulates in
-// fp32 and writes bf16; the expanded weight matrix never exists in memory.  Section "Reduce
-// intermediate and state traffic": gate/up projections fused with the gated activation; the
-// output projection fused with the routing score and the shared-expert result.
+// at a time on chip, multiplies it with the routed activation rows, accumulates in fp32 and
+// writes bf16; the expanded weight matrix never exists in memory.  Section "Match tile size to
+// expert load": the token side of a tile follows the expert's row count (16 to 128 rows), so
+// small expert groups cost little tensor work.  Section "Reduce intermediate and state
+// traffic": gate/up fused with the gated activation; the output projection fused with the
+// routing score and the shared-expert sum.
 //
-// GB300 design: one persistent CTA per SM; a tile is (expert, block of <= 128 token rows,
-// 256-row weight tile).  Each tcgen05.mma is M = 128 token rows x N = 256 weight rows x K = 16:
-//   gate/up  N = 128 gate rows + the same 128 up rows, so one accumulator row holds g and u of
-//            the token for 128 values of i;
-//   down     N = 256 rows of d; K runs over the hi half of h, then its lo half (h is carried to
-//            16 bits as a bf16 pair).
-// Warp roles (22 warps):
-//   warps 0-15  dequant: packed chunk pair (smem) -> bf16 B tile (256 rows x 64) in the 128-byte
-//               swizzled K-major layout the tensor core reads; w = fma.rn.bf16x2(q, scale, bias)
-//   warps 16-19 epilogue: TMEM -> registers; one token row per thread
-//   warp 20     producer: cp.async.bulk of 9216-byte weight pairs, TMA tiles of activations
-//   warp 21     MMA issuer (one thread) and TMEM owner (2 accumulators of 256 columns)
+// A tile is (expert, block of <= 128 token rows, weight tile).  Every MMA computes
+//     D[m][n] (+)= sum_k W[m][k] X[n][k]     M = 128 weight rows, N = 16 ceil(rows / 16), K = 16
+// with W, bf16, read from tensor memory (TMEM) and X, the block's token rows, read from shared
+// memory (128-byte swizzled, K-major).  Writing the dequantised weights to TMEM keeps them off
+// the shared-memory path entirely: shared memory carries only the packed codes, the token rows
+// and the tensor core's reads of the token rows.
+//   gate/up  two A matrices per K block: 128 gate rows and the same 128 up rows (i = 128 wt ..),
+//            so g and u of one (i, token) sit in the same TMEM lane and column of D_0 / D_1;
+//            h = silu(g) u is written as a bf16 hi/lo pair.
+//   down     two A matrices: output rows 256 wt .. +127 and +128 .. +255; h enters as its hi
+//            half and its lo half: for N <= 32 as one B operand of 2N rows (hi rows, then lo
+//            rows; y = D[n] + D[N + n]), else as two MMAs per K step into the same D; weight * y
+//            (fp32) leaves the chunk in one of two ways, chosen by whether the weighted rows fit
+//            well inside L2: stored into Y [d/256][(k+1)T][256] at the row index of h (the rows
+//            of a 32-token chunk are one contiguous block of a 256-column tile: one TMA bulk
+//            copy; plain stores, no atomics), or added into the fp32 token-order sum with one
+//            1 KB bulk reduce-add per token.
+// combine_rows sums each token's k routed rows and its shared row of Y in a fixed order.
+// Warp roles (28 warps):
+//   0-15  dequant, two sets of 8 warps taking alternate K blocks: warp w owns row 32 (w & 3) +
+//         lane of matrix (w >> 2) & 1; per K block a thread loads its 64 codes (two 16-byte
+//         loads), dequantises them exactly (eight words, one bf16x2 FMA per two weights) and
+//         writes the row with one tcgen05.st (32 columns)
+//   16-23 epilogue, two warps per TMEM lane quadrant taking alternate 16-token column groups:
+//         D -> registers (lane = weight row, column = token) -> token-major staging in shared
+//         memory -> 16-byte stores of h, or bulk copies / reduce-adds of weight * y
+//   24    codes producer: cp.async.bulk of the 9216-byte packed chunk pair of each K block
+//   25    token-row producer: TMA loads of the block's token rows (64-row boxes, then 16-row
+//         boxes for the rest)
+//   26-27 MMA issuers, one thread each: warp 26 + m issues every MMA into D_m (a warp issues a
+//         tcgen05.mma about every 54 cycles, while the tensor core finishes a 128 x N x 16 MMA
+//         with A in TMEM in N / 2 cycles: two issuers double the rate for small N); warp 26
+//         owns the TMEM allocation
+// TMEM (512 columns): A ring of 4 slots x 64 columns at columns 0..255 (slot s, matrix m, K step
+// ks at 64 s + 32 m + 8 ks); accumulators in two D slots of 128 columns at 256 and 384.  A tile
+// whose two accumulators fit in 128 columns (gate/up N <= 64; down N <= 64) takes one slot, so the next tile's MMAs run while the epilogue drains it; a larger tile
+// takes both (D_m in its own slot).  MMA threads and epilogue walk the same slot sequence.
+// Each MMA thread commits once per K block to a ring of "K block done" barriers (two arrivals);
+// the dequant sets (A slot reuse) and the token-row producer (token-row slot reuse) wait on it.
+// One "ready" barrier per K block collects the dequant set's warps and the token-row bytes, so
+// an MMA thread waits once per K block: the issuing threads set the pace.
 // All waits are bounded (MOE_STATUS_TIMEOUT, then the CTA unwinds).
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kDeqWarps = 16;
-constexpr int kEpiWarps = 4;
-constexpr int kProdWarp = kDeqWarps + kEpiWarps;   // 20
-constexpr int kMmaWarp = kProdWarp + 1;            // 21
-constexpr int kThreads = (kMmaWarp + 1) * 32;      // 704
+constexpr int kTmDeqSet = 8;                  // warps of one dequant set
+constexpr int kTmDeqWarps = 2 * kTmDeqSet;
+constexpr int kTmEpiWarp0 = kTmDeqWarps;      // 16
+constexpr int kTmEpiWarps = 8;                   // two per TMEM lane quadrant
+constexpr int kTmEpiThreads = kTmEpiWarps * 32;
+constexpr int kTmCodeWarp = kTmEpiWarp0 + kTmEpiWarps;
+constexpr int kTmXWarp = kTmCodeWarp + 1;
+constexpr int kTmMmaWarp = kTmXWarp + 1;                 // two MMA warps
+constexpr int kTmThreads = (kTmMmaWarp + 2) * 32;
 
-constexpr int kTokRows = 128;                      // MMA M: token rows of a tile
-constexpr int kWRows = 256;                        // MMA N: weight rows of a tile
-constexpr int kActBytes = kTokRows * 128;          // 128 rows x 64 bf16 (one K block)
-constexpr int kWdqBytes = kWRows * 128;            // 256 rows x 64 bf16
-constexpr int kRawBytes = kChunkPairBytes;         // 9216
-constexpr int kEpiRows = kEpiWarps * 32;           // token rows of the epilogue (one per thread)
-constexpr int kStageStride = 64 * 4 + 16;          // 64 fp32 + 16 bytes of padding (bank spread)
+constexpr int kTmA = 4;                       // A ring slots (TMEM)
+constexpr int kTmBox = 16;                    // token rows per small TMA box
+constexpr int kTmBoxL = 64;                   // token rows per large TMA box
+constexpr int kTmKD = 8;                      // "K block done" barriers
+constexpr int kTmXBytes = kMaxN * 128;        // token rows of one K block: 128 rows x 64 bf16
 
-#ifndef MOE_GU_RAW
-#define MOE_GU_RAW 4
-#endif
-#ifndef MOE_GU_WDQ
-#define MOE_GU_WDQ 4
-#endif
-#ifndef MOE_GU_ACT
-#define MOE_GU_ACT 3
-#endif
-#ifndef MOE_DN_RAW
-#define MOE_DN_RAW 3
-#endif
-#ifndef MOE_DN_WDQ
-#define MOE_DN_WDQ 3
-#endif
-#ifndef MOE_DN_ACT
-#define MOE_DN_ACT 4
-#endif
 template <bool kDown>
-struct Cfg {
-    static constexpr int RAW = kDown ? MOE_DN_RAW : MOE_GU_RAW;   // weight-pair ring (HBM -> smem)
-    static constexpr int WDQ = kDown ? MOE_DN_WDQ : MOE_GU_WDQ;   // dequantised weight ring
-    static constexpr int ACT = kDown ? MOE_DN_ACT : MOE_GU_ACT;   // activation ring (TMA)
-    static constexpr int PARTS = kDown ? 2 : 1;    // activation K steps per weight K block
-    static constexpr int act_off = 0;
-    static constexpr int wdq_off = act_off + ACT * kActBytes;
-    static constexpr int raw_off = wdq_off + WDQ * kWdqBytes;
-    // down: epilogue staging of 64 output columns per token row (row stride 272 bytes)
-    static constexpr int stage_off = raw_off + RAW * kRawBytes;
-    static constexpr int stage_bytes = kDown ? kEpiRows * kStageStride : 0;
-    static constexpr int bar_off = stage_off + stage_bytes;
+struct TmCfg {
+    static constexpr int RX = kDown ? 3 : 8;                 // token-row ring slots
+    static constexpr int RC = kDown ? 6 : 8;                 // packed-code ring slots
+    static constexpr int PARTS = kDown ? 2 : 1;              // hi, lo halves of h
+    static constexpr int XS = PARTS * kTmXBytes;             // bytes of a token-row slot
+    // staging of 32 tokens: gate/up bf16 [32][hi 128 | lo 128]; down two buffers of fp32 [32][256]
+    static constexpr int STAGE = kDown ? 2 * 32 * 1024 : 32 * 512;
+    static constexpr int x_off = 0;
+    static constexpr int c_off = x_off + RX * XS;
+    static constexpr int stage_off = c_off + RC * kChunkPairBytes;
+    static constexpr int tab_off = stage_off + STAGE;        // down: float weight[128], int token[128]
+    static constexpr int bar_off = tab_off + 1024;
 };
 
-struct Bars {
-    uint64_t raw_full[8], raw_empty[8], act_full[8], act_empty[8], wdq_full[6], wdq_empty[6];
-    uint64_t tm_full[2], tm_empty[2], drain;
+struct TmBars {
+    uint64_t c_full[8], c_empty[8], ready[kTmKD], kb_done[kTmKD];
+    uint64_t d_full[2], d_empty[2], drain[2];
     uint32_t tmem_slot;
     int abort;
 };
 
 template <bool kDown>
-constexpr int smem_bytes() {
-    return Cfg<kDown>::bar_off + (int)sizeof(Bars) + 1024;   // + alignment slack
+constexpr int tm_smem_bytes() {
+    return TmCfg<kDown>::bar_off + (int)sizeof(TmBars) + 1024;   // + alignment slack
 }
-static_assert(smem_bytes<false>() <= 232448, "gate/up smem");
-static_assert(smem_bytes<true>() <= 232448, "down smem");
+static_assert(tm_smem_bytes<false>() <= 232448, "gate/up smem");
+static_assert(tm_smem_bytes<true>() <= 232448, "down smem");
 
-// Weight chunks come from HBM and run up to RAW K blocks ahead of the activation tiles.
-// No deadlock: a wait on raw_empty for K block g needs the MMA of K block g - RAW - WDQ,
-// whose activation tiles were issued earlier.
-
-#ifdef MOE_TRACE
-constexpr int kTraceK = 96;
-#define TRACE(ev, g)                                                                     \
-    do {                                                                                 \
-        if (blockIdx.x == 0 && (g) < kTraceK) p.trace[(ev) * kTraceK + (g)] = clock64(); \
-    } while (0)
-#else
-#define TRACE(ev, g) \
-    do {             \
-    } while (0)
-#endif
-enum { TR_PRAW = 0, TR_PACT, TR_DWAIT, TR_DDONE, TR_MWAIT, TR_MDONE, TR_ETILE, TR_EDONE, TR_N };
-
-struct FfnParams {
+struct TmParams {
     const uint8_t* w_routed;   // packed stack: [E][tiles][K/64][2][4608]
     const uint8_t* w_shared;
     const int* mode_routed;    // scale encoding of each packed buffer (header word)
@@ -111,7 +110,9 @@ struct FfnParams {
     const int4* tiles;         // (expert, first row, rows, weight tile); expert == E: shared
     const int* num_tiles;
     uint16_t* H;               // [(k+1)T][2I] bf16, hi | lo
+    float* Y;                  // [d/256][(k+1)T][256] fp32 weighted down-projection rows
     float* acc;                // [T][d] fp32 token-order sum
+    int rows_out;              // down: 1 = store rows into Y, 0 = bulk reduce-add into acc
     const int32_t* perm;
     const float* topk_w;
     int* status;
@@ -119,64 +120,79 @@ struct FfnParams {
     int T, d, I, E, k;
 };
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-    const uint32_t s = smem_u32(p);
-    return p + ((1024u - (s & 1023u)) & 1023u);
+__device__ __forceinline__ int tile_n(int rows) { return (rows + 15) & ~15; }
+
+// D placement of a tile, from the running slot counter sc: TMEM columns of D_0 / D_1 and the
+// slot(s) they occupy.
+struct DSlots {
+    int s0, s1;
+    bool two;
+    uint32_t col0, col1;
+};
+// Down tiles of at most 32 token rows stack the hi and lo halves of h as one B operand of 2N
+// rows (one MMA per K step and matrix, y = D[n] + D[N + n]); larger ones run both halves into the
+// same accumulator (two MMAs).
+__device__ __forceinline__ bool down_stacked(int N) { return N <= 32; }
+
+__device__ __forceinline__ DSlots d_slots(uint32_t sc, int N, bool down) {
+    DSlots r;
+    const int w = down && down_stacked(N) ? 2 * N : N;   // columns of one accumulator
+    r.s0 = (int)(sc & 1);
+    r.two = 2 * w > 128;
+    r.s1 = r.two ? r.s0 ^ 1 : r.s0;
+    r.col0 = 256u + 128u * r.s0;
+    r.col1 = r.two ? 256u + 128u * r.s1 : r.col0 + w;
+    return r;
 }
 
-__device__ __forceinline__ void raise_abort(volatile int* abort, int* status) {
+// Tuning builds (MOE_TRACE): clock64 stamps of CTA 0's first K blocks / tiles.
+#ifdef MOE_TRACE
+constexpr int kTmTraceK = 96;
+#define TM_TRACE(ev, g)                                                                       \
+    do {                                                                                      \
+        if (blockIdx.x == 0 && (g) < kTmTraceK) p.trace[(ev) * kTmTraceK + (g)] = clock64(); \
+    } while (0)
+#else
+#define TM_TRACE(ev, g) \
+    do {                \
+    } while (0)
+#endif
+enum { TT_PC = 0, TT_PX, TT_DW, TT_DD, TT_DS, TT_MW, TT_MD, TT_ET, TT_ED };
+
+__device__ __forceinline__ void tm_abort(volatile int* abort, int* status) {
     *abort = 1;
     set_status(status, MOE_STATUS_TIMEOUT);
 }
 
-// Wait (bounded, not cut short by the abort flag) until the last `depth` arms of a ring's
-// full barriers have landed, so no bulk copy is still writing shared memory at exit.
-__device__ void drain_ring(uint64_t* full, int depth, uint32_t issued) {
+// Wait (bounded, not cut short by the abort flag) until the last `last` arms of a ring of
+// `ring` full barriers have completed, so no copy is still writing shared memory at exit.
+__device__ void tm_drain(uint64_t* full, int ring, int last, uint32_t issued) {
     int never = 0;
-    const uint32_t first = issued > (uint32_t)depth ? issued - depth : 0;
-    for (uint32_t i = first; i < issued; ++i) mbar_wait(&full[i % depth], (i / depth) & 1, &never);
+    const uint32_t first = issued > (uint32_t)last ? issued - last : 0;
+    for (uint32_t i = first; i < issued; ++i) mbar_wait(&full[i % ring], (i / ring) & 1, &never);
 }
 
-// Walks this CTA's (tile, K block, part) sequence.
-struct Cursor {
-    int tile, kb, part, num, KB, parts;
-    int4 t;
-    const int4* tiles;
-    __device__ __forceinline__ void init(const int4* tl, int n, int kbs, int nparts) {
-        tiles = tl; num = n; KB = kbs; parts = nparts;
-        tile = blockIdx.x; kb = 0; part = 0;
-        if (tile < num) t = tiles[tile];
-    }
-    __device__ __forceinline__ bool done() const { return tile >= num; }
-    __device__ __forceinline__ void next() {
-        if (++part < parts) return;
-        part = 0;
-        if (++kb < KB) return;
-        kb = 0;
-        tile += gridDim.x;
-        if (tile < num) t = tiles[tile];
-    }
-};
-
-// -------- dequant of 32 weights (one half row of a packed chunk) into the swizzled layout ----
+// One row of 64 weights: 16 bytes of codes per half K block, per-row scale and bias pairs.
 template <bool kDenorm>
-__device__ __forceinline__ void dequant_store4(uint4 codes, uint32_t s2, uint32_t b2, uint8_t* row_dst, int r,
-                                               int c0) {
-    const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
+__device__ __forceinline__ void dequant_row64(uint4 c0, uint4 c1, uint32_t s2, uint32_t b2, uint32_t (&v)[32]) {
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t v[4];
-        dequant_word<kDenorm>(words[q], s2, b2, v);
-        const int c = c0 + q;
-        const uint32_t addr = smem_u32(row_dst + ((c ^ (r & 7)) << 4));
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
-                     "r"(v[3])
-                     : "memory");
+    for (int q = 0; q < 8; ++q) {
+        uint32_t o[4];
+        dequant_word<kDenorm>(w[q], s2, b2, o);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[4 * q + u] = o[u];
     }
 }
 
-// Bulk add of `bytes` fp32 from shared memory into global memory (TMA reduction; 16-byte
-// aligned addresses, bytes % 16 == 0); completion tracked per thread by bulk groups.
+
+// Bulk copy of `bytes` from shared to global memory (16-byte aligned, bytes % 16 == 0);
+// completion tracked per thread by bulk groups.
+__device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
     asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
                  "r"(smem_u32(ssrc)), "r"(bytes)
@@ -184,289 +200,353 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssr
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    return (uint32_t)f32_to_bf16_rn(a) | ((uint32_t)f32_to_bf16_rn(b) << 16);
-}
-
-// ======================================================================================
-// The kernel: kDown == false -> gate/up + SwiGLU into h; true -> down + weighted fp32 sums.
-// tm_a: activations of routed rows (xs for gate/up, h for down); tm_b: the shared expert's
-// activation rows (x for gate/up; unused for down, whose shared rows follow in h).
-// ======================================================================================
 template <bool kDown>
-__global__ void __launch_bounds__(kThreads, 1)
-    ffn_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, FfnParams p) {
-    using C = Cfg<kDown>;
+__global__ void __launch_bounds__(kTmThreads, 1)
+    ffn_tm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_al,
+                  const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_bl, TmParams p) {
+    using C = TmCfg<kDown>;
     extern __shared__ uint8_t smem_dyn[];
     const int num = *p.num_tiles;
     if ((int)blockIdx.x >= num) return;
-    uint8_t* smem = align1024(smem_dyn);
-    uint8_t* act = smem + C::act_off;
-    uint8_t* wdq = smem + C::wdq_off;
-    uint8_t* raw = smem + C::raw_off;
-    Bars* bars = reinterpret_cast<Bars*>(smem + C::bar_off);
-    volatile int* abort = &bars->abort;
+    uint8_t* smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+    uint8_t* xring = smem + C::x_off;
+    uint8_t* cring = smem + C::c_off;
+    TmBars* b = reinterpret_cast<TmBars*>(smem + C::bar_off);
+    volatile int* abort = &b->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int KB = (kDown ? p.I : p.d) / kBK;                  // weight K blocks
-    const int WT = (kDown ? p.d : p.I * 2) / kWRows;          // weight tiles per expert
+    const int KB = (kDown ? p.I : p.d) / kBK;                 // weight K blocks
+    const int WT = kDown ? p.d / 256 : p.I / kTileRows;      // weight tiles per expert
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::RAW; ++i) { mbar_init(&bars->raw_full[i], 1); mbar_init(&bars->raw_empty[i], kDeqWarps); }
-        for (int i = 0; i < C::ACT; ++i) { mbar_init(&bars->act_full[i], 1); mbar_init(&bars->act_empty[i], 1); }
-        for (int i = 0; i < C::WDQ; ++i) { mbar_init(&bars->wdq_full[i], kDeqWarps); mbar_init(&bars->wdq_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&bars->tm_full[i], 1); mbar_init(&bars->tm_empty[i], kEpiWarps); }
-        mbar_init(&bars->drain, 1);
-        bars->abort = 0;
+        for (int i = 0; i < C::RC; ++i) { mbar_init(&b->c_full[i], 1); mbar_init(&b->c_empty[i], kTmDeqSet); }
+        // ready: the 8 dequant warps of a K block's set + the token-row producer (with its bytes)
+        for (int i = 0; i < kTmKD; ++i) { mbar_init(&b->ready[i], kTmDeqSet + 1); mbar_init(&b->kb_done[i], 2); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&b->d_full[i], 2); mbar_init(&b->d_empty[i], kTmEpiWarps); }
+        mbar_init(&b->drain[0], 1);
+        mbar_init(&b->drain[1], 1);
+        b->abort = 0;
         fence_barrier_init();
     }
-    if (warp == kProdWarp && lane == 0) { prefetch_tmap(&tm_a); if (!kDown) prefetch_tmap(&tm_b); }
-    if (warp == kMmaWarp) { tmem_alloc(&bars->tmem_slot, 512); tmem_relinquish(); }
+    if (warp == kTmXWarp && lane == 0) {
+        prefetch_tmap(&tm_a);
+        prefetch_tmap(&tm_al);
+        if (!kDown) { prefetch_tmap(&tm_b); prefetch_tmap(&tm_bl); }
+    }
+    if (warp == kTmMmaWarp) { tmem_alloc(&b->tmem_slot, 512); tmem_relinquish(); }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = bars->tmem_slot;
+    const uint32_t tmem = b->tmem_slot;
 
-    if (warp == kProdWarp) {
+    if (warp == kTmCodeWarp) {
+        // packed codes of every (tile, K block), up to RC K blocks ahead of the dequant
         if (lane == 0) {
-            uint32_t rit = 0, ait = 0;
+            uint32_t it = 0;
             bool ok = true;
-            Cursor cr, ca;
-            cr.init(p.tiles, num, KB, 1);
-            ca.init(p.tiles, num, KB, C::PARTS);
-            while (ok && !ca.done()) {
-                while (ok && !cr.done() && rit < ait / C::PARTS + C::RAW) {
-                    const int e = cr.t.x, wt = cr.t.w;
-                    const uint8_t* w = (e < p.E ? p.w_routed + (size_t)(e * WT + wt) * KB * kRawBytes
-                                                : p.w_shared + (size_t)wt * KB * kRawBytes) +
-                                       (size_t)cr.kb * kRawBytes;
-                    const int rs = rit % C::RAW;
-                    if (!mbar_wait(&bars->raw_empty[rs], ((rit / C::RAW) & 1) ^ 1, abort)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&bars->raw_full[rs], kRawBytes);
-                    bulk_g2s(raw + rs * kRawBytes, w, kRawBytes, &bars->raw_full[rs]);
-                    TRACE(TR_PRAW, rit);
-                    ++rit;
-                    cr.next();
+            for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
+                const int4 t = p.tiles[tile];
+                const uint8_t* w = t.x < p.E ? p.w_routed + (size_t)(t.x * WT + t.w) * KB * kChunkPairBytes
+                                             : p.w_shared + (size_t)t.w * KB * kChunkPairBytes;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int cs = it % C::RC;
+                    if (!mbar_wait(&b->c_empty[cs], ((it / C::RC) & 1) ^ 1, abort)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&b->c_full[cs], kChunkPairBytes);
+                    bulk_g2s(cring + cs * kChunkPairBytes, w + (size_t)kb * kChunkPairBytes, kChunkPairBytes,
+                             &b->c_full[cs]);
+                    TM_TRACE(TT_PC, it);
                 }
-                if (!ok) break;
-                const int e = ca.t.x, row0 = ca.t.y;
-                const int as = ait % C::ACT;
-                if (!mbar_wait(&bars->act_empty[as], ((ait / C::ACT) & 1) ^ 1, abort)) { ok = false; break; }
-                mbar_arrive_expect_tx(&bars->act_full[as], kActBytes);
-                if (kDown) {
-                    const int hrow0 = e < p.E ? row0 : p.k * p.T + row0;
-                    tma_load_2d(act + as * kActBytes, &tm_a, ca.part * p.I + ca.kb * kBK, hrow0, &bars->act_full[as]);
-                } else {
-                    tma_load_2d(act + as * kActBytes, e < p.E ? &tm_a : &tm_b, ca.kb * kBK, row0, &bars->act_full[as]);
-                }
-                TRACE(TR_PACT, ait);
-                ++ait;
-                ca.next();
             }
-            if (!ok) raise_abort(abort, p.status);
-            drain_ring(bars->raw_full, C::RAW, rit);
-            drain_ring(bars->act_full, C::ACT, ait);
+            if (!ok) tm_abort(abort, p.status);
+            tm_drain(b->c_full, C::RC, C::RC, it);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kTmXWarp) {
+        // token rows of every (tile, K block), up to RX K blocks ahead of the MMA; for the down
+        // projection the lo half of h follows the hi rows directly when the tile stacks (N <= 32)
         if (lane == 0) {
-            uint32_t wit = 0, ait = 0, tcount = 0;
-            uint32_t use[2] = {0, 0};
+            uint32_t it = 0;
             bool ok = true;
-            const uint32_t act_base = smem_u32(act), wdq_base = smem_u32(wdq);
-            const uint32_t idesc = idesc_bf16_f32(kTokRows, kWRows);
-            for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x, ++tcount) {
-                const int buf = tcount & 1;
-                if (!mbar_wait(&bars->tm_empty[buf], (use[buf] & 1) ^ 1, abort)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t dcol = tmem + 256u * buf;
-                for (int kb = 0; kb < KB && ok; ++kb) {
-                    const int ws = wit % C::WDQ;
-                    if (!mbar_wait(&bars->wdq_full[ws], (wit / C::WDQ) & 1, abort)) { ok = false; break; }
-                    TRACE(TR_MWAIT, wit);
-                    for (int part = 0; part < C::PARTS; ++part) {
-                        const int as = ait % C::ACT;
-                        if (!mbar_wait(&bars->act_full[as], (ait / C::ACT) & 1, abort)) { ok = false; break; }
-                        tc_fence_after();
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t ad = sw128_desc(act_base + as * kActBytes + ks * 32);
-                            const uint64_t bd = sw128_desc(wdq_base + ws * kWdqBytes + ks * 32);
-                            tc_mma_bf16(dcol, ad, bd, idesc, (kb | part | ks) ? 1u : 0u);
-                        }
-                        tc_commit(&bars->act_empty[as]);
-                        ++ait;
+            for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
+                const int4 t = p.tiles[tile];
+                const int e = t.x, row0 = t.y, N = tile_n(t.z);
+                const int xrow0 = kDown ? (e < p.E ? row0 : p.k * p.T + row0) : row0;
+                const CUtensorMap* tms = (kDown || e < p.E) ? &tm_a : &tm_b;
+                const CUtensorMap* tml = (kDown || e < p.E) ? &tm_al : &tm_bl;
+                const int lo_off = down_stacked(N) ? N * 128 : kTmXBytes;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int xs = it % C::RX;
+                    if (it >= (uint32_t)C::RX) {
+                        const uint32_t g = it - C::RX;
+                        if (!mbar_wait(&b->kb_done[g % kTmKD], (g / kTmKD) & 1, abort)) { ok = false; break; }
                     }
-                    tc_commit(&bars->wdq_empty[ws]);
-                    TRACE(TR_MDONE, wit);
-                    ++wit;
+                    // (the wait above also means that the ready barrier's phase for K block
+                    // it - 8 has completed: its MMAs were issued)
+                    uint64_t* rdy = &b->ready[it % kTmKD];
+                    mbar_arrive_expect_tx(rdy, C::PARTS * N * 128);
+                    uint8_t* dst = xring + xs * C::XS;
+                    for (int part = 0; part < C::PARTS; ++part) {
+                        const int x = part * p.I + kb * kBK;
+                        int r = 0;
+                        for (; r + kTmBoxL <= N; r += kTmBoxL)
+                            tma_load_2d(dst + part * lo_off + r * 128, tml, x, xrow0 + r, rdy);
+                        for (; r < N; r += kTmBox)
+                            tma_load_2d(dst + part * lo_off + r * 128, tms, x, xrow0 + r, rdy);
+                    }
+                    TM_TRACE(TT_PX, it);
+                }
+            }
+            if (!ok) tm_abort(abort, p.status);
+            tm_drain(b->ready, kTmKD, C::RX, it);   // the token rows of the last RX blocks have landed
+        }
+    } else if (warp >= kTmMmaWarp) {
+        if (lane == 0) {
+            const int m = warp - kTmMmaWarp;   // this thread's accumulator D_m and A matrix m
+            uint32_t it = 0, tcount = 0, sc = 0, use[2] = {0, 0};
+            bool ok = true;
+            const uint64_t xdesc0 = sw128_desc(smem_u32(xring));   // start address advances 16 B per unit
+            for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x, ++tcount) {
+                const int N = tile_n(p.tiles[tile].z);
+                const bool stacked = kDown && down_stacked(N);   // hi and lo rows as one B operand of 2N rows
+                const uint32_t idesc = idesc_bf16_f32(128, stacked ? 2 * N : N);
+                const DSlots ds = d_slots(sc, N, kDown);
+                if (!mbar_wait(&b->d_empty[ds.s0], (use[ds.s0] & 1) ^ 1, abort) ||
+                    (ds.two && !mbar_wait(&b->d_empty[ds.s1], (use[ds.s1] & 1) ^ 1, abort))) { ok = false; break; }
+                tc_fence_after();
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int as = it % kTmA, xs = it % C::RX;
+                    if (!mbar_wait(&b->ready[it % kTmKD], (it / kTmKD) & 1, abort)) { ok = false; break; }
+                    tc_fence_after();
+                    if (m == 0) TM_TRACE(TT_MW, it);
+                    const uint64_t xd = xdesc0 + (uint64_t)((xs * C::XS) >> 4);
+                    const uint32_t a0 = tmem + 64u * as + 32u * m, dm = tmem + (m ? ds.col1 : ds.col0);
+                    const int parts = stacked ? 1 : C::PARTS;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        for (int part = 0; part < parts; ++part)
+                            tc_mma_bf16_ts(dm, a0 + 8u * ks, xd + (uint64_t)((part * kTmXBytes + ks * 32) >> 4), idesc,
+                                           (kb | ks | part) ? 1u : 0u);
+                    }
+                    tc_commit(&b->kb_done[it % kTmKD]);
+                    if (m == 0) TM_TRACE(TT_MD, it);
                 }
                 if (!ok) break;
-                tc_commit(&bars->tm_full[buf]);
-                use[buf]++;
+                tc_commit(&b->d_full[ds.s0]);
+                if (ds.two) tc_commit(&b->d_full[ds.s1]);
+                use[ds.s0]++;
+                if (ds.two) use[ds.s1]++;
+                sc += ds.two ? 2 : 1;
             }
-            if (!ok) raise_abort(abort, p.status);
-            tc_commit(&bars->drain);
+            if (!ok) tm_abort(abort, p.status);
+            tc_commit(&b->drain[m]);
             int never = 0;
-            mbar_wait(&bars->drain, 0, &never);
+            mbar_wait(&b->drain[m], 0, &never);
         }
-    } else if (warp < kDeqWarps) {
-        // dequant: thread -> (weight row r of the 256-row tile, half hf); 32 weights per K block.
-        // Rows 0..127 come from the first chunk of the pair, rows 128..255 from the second.
-        // Every warp waits on its own (lock-stepping the 16 warps on a named barrier measured
-        // slower: a warp may start the next K block while others finish this one).
-        const int r = threadIdx.x & 255, hf = threadIdx.x >> 8;
-        const int mat = r >> 7, rr = r & 127;
-        const uint32_t code_off = mat * kChunkBytes + hf * 2048 + rr * 16;
-        const uint32_t sb_off = mat * kChunkBytes + kChunkCodes + 2 * rr;
-        const uint32_t row_off = (r >> 3) * 1024 + (r & 7) * 128;
-        uint32_t rit = 0;
-        bool ok = true;
+    } else if (warp < kTmDeqWarps) {
+        // dequant: set (warp >> 3) takes the K blocks of its parity; thread -> row r of matrix m
+        const int set = warp >> 3, m = (warp >> 2) & 1, q = warp & 3, r = 32 * q + lane;
+        const uint32_t code_off = m * kChunkBytes + r * 16;
+        const uint32_t sb_off = m * kChunkBytes + kChunkCodes + 2 * r;
+        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + 32u * m;
         const int mode_r = *p.mode_routed, mode_s = *p.mode_shared;
+        uint32_t it = 0;
+        bool ok = true;
         for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
-            const bool denorm = (p.tiles[tile].x < p.E ? mode_r : mode_s) == kScaleDenorm;
-            for (int kb = 0; kb < KB; ++kb) {
-                const int rs = rit % C::RAW, ws = rit % C::WDQ;
-                const bool got = mbar_wait(&bars->raw_full[rs], (rit / C::RAW) & 1, abort) &&
-                                 mbar_wait(&bars->wdq_empty[ws], ((rit / C::WDQ) & 1) ^ 1, abort);
+            const bool denorm = __all_sync(0xffffffffu, (p.tiles[tile].x < p.E ? mode_r : mode_s) == kScaleDenorm);
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                if ((int)(it & 1) != set) continue;
+                const int cs = it % C::RC, as = it % kTmA;
+                const uint32_t g = it - kTmA;   // the K block that last used this A slot
+                const bool got = mbar_wait(&b->c_full[cs], (it / C::RC) & 1, abort) &&
+                                 (it < (uint32_t)kTmA || mbar_wait(&b->kb_done[g % kTmKD], (g / kTmKD) & 1, abort));
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                if (threadIdx.x == 0) TRACE(TR_DWAIT, rit);
-                const uint8_t* ch = raw + rs * kRawBytes;
-                const uint4 cw = *reinterpret_cast<const uint4*>(ch + code_off);
-                const uint32_t sv = *reinterpret_cast<const uint16_t*>(ch + sb_off);
-                const uint32_t bv = *reinterpret_cast<const uint16_t*>(ch + sb_off + 256);
-                if (denorm)
-                    dequant_store4<true>(cw, sv * 0x10001u, bv * 0x10001u, wdq + ws * kWdqBytes + row_off, r, 4 * hf);
-                else
-                    dequant_store4<false>(cw, sv * 0x10001u, bv * 0x10001u, wdq + ws * kWdqBytes + row_off, r, 4 * hf);
-                fence_proxy_async_smem();
+                if (threadIdx.x == 0) TM_TRACE(TT_DW, it);
+                const uint8_t* ch = cring + cs * kChunkPairBytes;
+                const uint4 c0 = *reinterpret_cast<const uint4*>(ch + code_off);
+                const uint4 c1 = *reinterpret_cast<const uint4*>(ch + code_off + 2048);
+                const uint32_t s2 = *reinterpret_cast<const uint16_t*>(ch + sb_off) * 0x10001u;
+                const uint32_t b2 = *reinterpret_cast<const uint16_t*>(ch + sb_off + 256) * 0x10001u;
+                uint32_t v[32];
+                if (denorm) dequant_row64<true>(c0, c1, s2, b2, v);
+                else dequant_row64<false>(c0, c1, s2, b2, v);
                 __syncwarp();
-                if (lane == 0) { mbar_arrive(&bars->raw_empty[rs]); mbar_arrive(&bars->wdq_full[ws]); }
-                if (threadIdx.x == 0) TRACE(TR_DDONE, rit);
-                ++rit;
+                if (threadIdx.x == 0) TM_TRACE(TT_DD, it);
+                if (lane == 0) mbar_arrive(&b->c_empty[cs]);
+                tc_fence_after();   // the MMAs that read this A slot before have completed
+                tmem_st32(trow + 64u * as, v);
+                tmem_st_wait();
+                if (threadIdx.x == 0) TM_TRACE(TT_DS, it);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&b->ready[it % kTmKD]);
             }
         }
-        if (!ok && lane == 0) raise_abort(abort, p.status);
-    } else {
-        // epilogue: thread = token row (32 per warp, warp w % 4 = TMEM lane quadrant).  Its first
-        // thread waits for the accumulator and releases the 4 warps through a named barrier.
-        const int q = warp & 3;
-        uint32_t use[2] = {0, 0}, tcount = 0;
+        if (!ok && lane == 0) tm_abort(abort, p.status);
+    } else if (warp < kTmCodeWarp) {
+        // epilogue: thread -> weight row r of D_0 and D_1 (TMEM lane quadrant warp & 3); warp
+        // group `half` takes the 16-token column groups of its parity.  32 tokens at a time are
+        // staged token-major in shared memory, then written out: h with 16-byte stores by all
+        // epilogue threads; weight * y as one bulk copy (the chunk's 32 rows of one 256-column
+        // tile of Y are one contiguous block).
+        const int q = warp & 3, half = (warp - kTmEpiWarp0) >> 2, r = 32 * q + lane, et = threadIdx.x - kTmEpiWarp0 * 32;
+        uint8_t* stage = smem + C::stage_off;
+        float* s_w = reinterpret_cast<float*>(smem + C::tab_off);
+        int* s_tok = reinterpret_cast<int*>(smem + C::tab_off + 512);
+        const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
+        const size_t yrows = (size_t)(p.k + 1) * p.T;
+        uint32_t tcount = 0, chunk = 0, sc = 0, use[2] = {0, 0};
         bool ok = true;
         for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x, ++tcount) {
             const int4 t = p.tiles[tile];
-            const int e = t.x, row0 = t.y, rows = t.z, wt = t.w;
-            const int buf = tcount & 1;
-            if (threadIdx.x == kDeqWarps * 32 && !mbar_wait(&bars->tm_full[buf], use[buf] & 1, abort))
-                raise_abort(abort, p.status);
-            named_bar_sync(2, kEpiWarps * 32);
+            const int e = t.x, row0 = t.y, rows = t.z, wt = t.w, N = tile_n(rows);
+            const size_t orow0 = e < p.E ? (size_t)row0 : (size_t)p.k * p.T + row0;   // row of H / Y
+            if (kDown && et < rows) {
+                const int asg = e < p.E ? p.perm[row0 + et] : 0;
+                s_w[et] = e < p.E ? p.topk_w[asg] : 1.0f;
+                s_tok[et] = e < p.E ? asg / p.k : row0 + et;
+            }
+            const DSlots ds = d_slots(sc, N, kDown);
+            if (et == 0 && (!mbar_wait(&b->d_full[ds.s0], use[ds.s0] & 1, abort) ||
+                            (ds.two && !mbar_wait(&b->d_full[ds.s1], use[ds.s1] & 1, abort))))
+                tm_abort(abort, p.status);
+            named_bar_sync(2, kTmEpiThreads);
             if (*abort) { ok = false; break; }
             tc_fence_after();
-            if (warp == kDeqWarps && lane == 0) TRACE(TR_ETILE, tcount);
-            const int tok = 32 * q + lane;                        // row within the tile
-            const bool live = tok < rows;
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + 256u * buf;
-            if (!kDown) {
-                // columns 0..127: g for i = 128*wt + c; columns 128..255: u for the same i
-                const size_t hrow = e < p.E ? (size_t)row0 + tok : (size_t)p.k * p.T + row0 + tok;
-                uint16_t* hp = p.H + hrow * 2 * p.I + (size_t)wt * 128;
-                for (int c = 0; c < 8; ++c) {
+            const uint32_t td0 = tlane + ds.col0, td1 = tlane + ds.col1;   // this lane quadrant's D_0, D_1
+            if (et == 0) TM_TRACE(TT_ET, tcount);
+            for (int c0 = 0; c0 < N; c0 += 32, ++chunk) {
+                const int c = c0 + 16 * half;          // this warp's 16 tokens: c .. c+15
+                const bool last = c0 + 32 >= N;
+                if (!kDown) {
+                    uint16_t* st = reinterpret_cast<uint16_t*>(stage);   // [32][hi 128 | lo 128]
                     uint32_t G[16], U[16];
-                    tmem_ld16(taddr + 16 * c, G);
-                    tmem_ld16(taddr + 128 + 16 * c, U);
-                    tmem_ld_wait();
-                    uint32_t hi[8], lo[8];
-#pragma unroll
-                    for (int jj = 0; jj < 16; jj += 2) {
-                        float hv[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const float gv = __uint_as_float(G[jj + u]), uv = __uint_as_float(U[jj + u]);
-                            hv[u] = gv / (1.0f + __expf(-gv)) * uv;
-                        }
-                        const uint32_t h2 = pack_bf16(hv[0], hv[1]);
-                        hi[jj / 2] = h2;
-                        lo[jj / 2] = pack_bf16(hv[0] - bf16lo(h2), hv[1] - bf16hi(h2));
-                    }
-                    if (live) {
-                        uint4* dh = reinterpret_cast<uint4*>(hp + 16 * c);
-                        uint4* dl = reinterpret_cast<uint4*>(hp + p.I + 16 * c);
-                        dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-                        dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                        dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-                    }
-                }
-            } else {
-                // 256 columns of d starting at 256*wt: acc[token][n] += w * y, 64 columns at a time
-                // through the thread's staging row and one bulk reduce-add (TMA) per piece
-                int tk = 0;
-                float w = 0.f;
-                if (live) {
-                    if (e < p.E) {
-                        const int asg = p.perm[row0 + tok];
-                        tk = asg / p.k;
-                        w = p.topk_w[asg];
-                    } else {
-                        tk = row0 + tok;
-                        w = 1.0f;
-                    }
-                }
-                float* ap = p.acc + (size_t)tk * p.d + (size_t)wt * kWRows;
-                uint8_t* srow = smem + C::stage_off + (32 * q + lane) * kStageStride;
-                for (int pc = 0; pc < 4; ++pc) {
-                    bulk_wait_read0();   // the previous piece has left the staging row
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t Y[16];
-                        tmem_ld16(taddr + 64 * pc + 16 * c, Y);
+                    if (c < N) {
+                        tmem_ld16(td0 + c, G);
+                        tmem_ld16(td1 + c, U);
                         tmem_ld_wait();
+                    }
+                    if (last) {   // D is no longer read: the next tile's MMAs may start
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(&b->d_empty[ds.s0]);
+                            if (ds.two) mbar_arrive(&b->d_empty[ds.s1]);
+                        }
+                    }
+                    if (c < N) {
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const uint32_t a = smem_u32(srow + 64 * c + 16 * v);
-                            asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a),
-                                         "f"(w * __uint_as_float(Y[4 * v])), "f"(w * __uint_as_float(Y[4 * v + 1])),
-                                         "f"(w * __uint_as_float(Y[4 * v + 2])), "f"(w * __uint_as_float(Y[4 * v + 3]))
-                                         : "memory");
+                        for (int u = 0; u < 16; ++u) {
+                            const float gv = __uint_as_float(G[u]), uv = __uint_as_float(U[u]);
+                            const float h = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                            const uint16_t hi = f32_to_bf16_rn(h);
+                            const int n = 16 * half + u;
+                            st[n * 256 + r] = hi;
+                            st[n * 256 + 128 + r] = f32_to_bf16_rn(h - __uint_as_float((uint32_t)hi << 16));
+                        }
+                    }
+                    named_bar_sync(2, kTmEpiThreads);
+                    // tokens c0 .. c0+31: 32 pieces of 16 bytes each (16 hi, 16 lo)
+                    for (int pi = et; pi < 32 * 32; pi += kTmEpiThreads) {
+                        const int n = pi >> 5, pc = pi & 31, tok = c0 + n;
+                        if (tok < rows) {
+                            const int col = (pc < 16 ? 0 : p.I - 128) + wt * 128 + 8 * pc;
+                            *reinterpret_cast<uint4*>(p.H + (orow0 + tok) * 2 * p.I + col) =
+                                *reinterpret_cast<const uint4*>(st + n * 256 + 8 * pc);
+                        }
+                    }
+                    named_bar_sync(2, kTmEpiThreads);
+                } else {
+                    // two staging buffers, alternate chunks: a chunk's bulk copy reads one while
+                    // the next chunk is written into the other
+                    float* st = reinterpret_cast<float*>(stage) + (chunk & 1) * (32 * 256);   // [32][256]
+                    if (c < N) {
+                        const bool stacked = down_stacked(N);   // the lo half's products sit N columns further
+#pragma unroll
+                        for (int m = 0; m < 2; ++m) {
+                            uint32_t R[16], L[16];
+                            const uint32_t tdm = m ? td1 : td0;
+                            tmem_ld16(tdm + c, R);
+                            if (stacked) tmem_ld16(tdm + N + c, L);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) {
+                                const float w = c + u < rows ? s_w[c + u] : 0.0f;
+                                const float y = __uint_as_float(R[u]) + (stacked ? __uint_as_float(L[u]) : 0.0f);
+                                st[(16 * half + u) * 256 + 128 * m + r] = w * y;
+                            }
+                        }
+                    }
+                    if (last) {   // D is no longer read: the next tile's MMAs may start
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(&b->d_empty[ds.s0]);
+                            if (ds.two) mbar_arrive(&b->d_empty[ds.s1]);
                         }
                     }
                     fence_proxy_async_smem();
-                    if (live) {
-                        bulk_reduce_add_f32(ap + 64 * pc, srow, 256);
-                        bulk_commit();
+                    named_bar_sync(2, kTmEpiThreads);
+                    const int nv = rows - c0 < 32 ? rows - c0 : 32;   // rows of this chunk
+                    if (p.rows_out) {
+                        if (et == 0) {
+                            bulk_s2g(p.Y + ((size_t)wt * yrows + orow0 + c0) * 256, st, (uint32_t)nv * 1024);
+                            bulk_commit();
+                            bulk_wait_read1();   // the previous chunk (the other buffer) has been read
+                        }
+                    } else if (lane < 4) {
+                        // token n = (epilogue warp) + 8 lane: its 1 KB row added into acc; the
+                        // issues are spread over the eight warps
+                        const int n = (warp - kTmEpiWarp0) + 8 * lane;
+                        if (n < nv) {
+                            bulk_reduce_add_f32(p.acc + (size_t)s_tok[c0 + n] * p.d + (size_t)wt * 256, st + n * 256,
+                                                1024);
+                            bulk_commit();
+                            bulk_wait_read1();   // this lane's previous chunk has been read
+                        } else {
+                            bulk_wait_read0();
+                        }
                     }
+                    named_bar_sync(2, kTmEpiThreads);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (warp == kDeqWarps && lane == 0) TRACE(TR_EDONE, tcount);
-            if (lane == 0) mbar_arrive(&bars->tm_empty[buf]);
-            use[buf]++;
+            if (et == 0) TM_TRACE(TT_ED, tcount);
+            use[ds.s0]++;
+            if (ds.two) use[ds.s1]++;
+            sc += ds.two ? 2 : 1;
         }
-        if (!ok && lane == 0) raise_abort(abort, p.status);
-        if (kDown) bulk_wait0();   // every bulk reduce-add of this thread has completed
+        if (!ok && lane == 0) tm_abort(abort, p.status);
+        if (kDown && (et == 0 || lane < 4)) bulk_wait0();   // every bulk copy / reduce-add has completed
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+    if (warp == kTmMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-// ======================================================================================
-// combine: y = bf16(acc)
-// ======================================================================================
-// y = bf16(sum); the sum is left at zero (the one-launch decode kernel relies on that)
-__global__ void combine_kernel(float4* __restrict__ acc, uint2* __restrict__ y, size_t n4) {
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-        const float4 v = acc[i];
-        y[i] = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
-        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+// y[t] = bf16( sum_j Y[pos[t k + j]] + Y[k T + t] ), j = 0..k-1 in order, then the shared row;
+// Y is [d/256][(k+1)T][256]; one thread per 4 columns of a token (16-byte loads, 8-byte store).
+__global__ void combine_rows_kernel(const float4* __restrict__ Y, const int32_t* __restrict__ pos,
+                                    uint2* __restrict__ y, int T, int d4, int k) {
+    const size_t n = (size_t)T * d4, tile4 = (size_t)(k + 1) * T * 64;   // float4s of a 256-column tile
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / d4), c = (int)(i % d4);
+        const float4* Yc = Y + (size_t)(c >> 6) * tile4 + (c & 63);
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float4 v = __ldcs(Yc + (size_t)pos[(size_t)t * k + j] * 64);
+            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        }
+        const float4 v = __ldcs(Yc + ((size_t)k * T + t) * 64);
+        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        y[i] = make_uint2((uint32_t)f32_to_bf16_rn(s.x) | ((uint32_t)f32_to_bf16_rn(s.y) << 16),
+                          (uint32_t)f32_to_bf16_rn(s.z) | ((uint32_t)f32_to_bf16_rn(s.w) << 16));
     }
 }
 
-FfnParams make_params(const FfnArgs& a, bool gate_up) {
-    FfnParams p{};
+TmParams make_tm_params(const FfnArgs& a, bool gate_up) {
+    TmParams p{};
     // packed buffer: header, gate/up pairs, down pairs
     const size_t gu_bytes = (size_t)(a.I / kTileRows) * (a.d / kBK) * kChunkPairBytes;
     p.w_routed = a.w_routed + kPackHeader + (gate_up ? 0 : (size_t)a.E * gu_bytes);
@@ -476,7 +556,9 @@ FfnParams make_params(const FfnArgs& a, bool gate_up) {
     p.tiles = reinterpret_cast<const int4*>(a.ws + (gate_up ? a.L.gu_tiles : a.L.dn_tiles));
     p.num_tiles = reinterpret_cast<const int*>(a.ws + (gate_up ? a.L.gu_num : a.L.dn_num));
     p.H = reinterpret_cast<uint16_t*>(a.ws + a.L.H);
+    p.Y = reinterpret_cast<float*>(a.ws + a.L.Y);
     p.acc = reinterpret_cast<float*>(a.ws + a.L.acc);
+    p.rows_out = ffn_rows_output(a.T, a.d, a.k) ? 1 : 0;
     p.perm = a.perm;
     p.topk_w = a.topk_w;
     p.status = reinterpret_cast<int*>(a.ws + a.L.status);
@@ -488,48 +570,85 @@ FfnParams make_params(const FfnArgs& a, bool gate_up) {
 }
 
 template <bool kDown>
-cudaError_t set_smem_attr() {
+cudaError_t set_tm_smem_attr() {
     static bool done = false;
     if (done) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(ffn_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           smem_bytes<kDown>());
+    cudaError_t err = cudaFuncSetAttribute(ffn_tm_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           tm_smem_bytes<kDown>());
     if (err == cudaSuccess) done = true;
     return err;
 }
 
 }  // namespace
 
-cudaError_t launch_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches) {
-    cudaError_t err = set_smem_attr<false>();
+cudaError_t launch_gate_up_tm(const FfnArgs& a, cudaStream_t st, unsigned long long* launches) {
+    cudaError_t err = set_tm_smem_attr<false>();
     if (err != cudaSuccess) return err;
-    CUtensorMap tm_xs, tm_x;
-    err = make_tmap_bf16_2d(&tm_xs, a.ws + a.L.xs, (uint64_t)a.k * a.T, a.d, (uint64_t)a.d * 2, kBK, kTokRows);
+    CUtensorMap tm_xs, tm_xsl, tm_x, tm_xl;
+    err = make_tmap_bf16_2d(&tm_xs, a.ws + a.L.xs, (uint64_t)a.k * a.T, a.d, (uint64_t)a.d * 2, kBK, kTmBox);
+    if (err == cudaSuccess)
+        err = make_tmap_bf16_2d(&tm_xsl, a.ws + a.L.xs, (uint64_t)a.k * a.T, a.d, (uint64_t)a.d * 2, kBK, kTmBoxL);
+    if (err == cudaSuccess) err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, kTmBox);
+    if (err == cudaSuccess) err = make_tmap_bf16_2d(&tm_xl, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, kTmBoxL);
     if (err != cudaSuccess) return err;
-    err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, kTokRows);
-    if (err != cudaSuccess) return err;
-    ffn_kernel<false><<<a.num_sms, kThreads, smem_bytes<false>(), st>>>(tm_xs, tm_x, make_params(a, true));
+    ffn_tm_kernel<false><<<a.num_sms, kTmThreads, tm_smem_bytes<false>(), st>>>(tm_xs, tm_xsl, tm_x, tm_xl,
+                                                                              make_tm_params(a, true));
     *launches += 1;
     return cudaGetLastError();
 }
 
-cudaError_t launch_down(const FfnArgs& a, cudaStream_t st, unsigned long long* launches) {
-    cudaError_t err = set_smem_attr<true>();
+cudaError_t launch_down_tm(const FfnArgs& a, cudaStream_t st, unsigned long long* launches) {
+    cudaError_t err = set_tm_smem_attr<true>();
     if (err != cudaSuccess) return err;
-    CUtensorMap tm_h;
+    CUtensorMap tm_h, tm_hl;
     err = make_tmap_bf16_2d(&tm_h, a.ws + a.L.H, (uint64_t)(a.k + 1) * a.T, 2 * (uint64_t)a.I, (uint64_t)a.I * 4,
-                            kBK, kTokRows);
+                            kBK, kTmBox);
+    if (err == cudaSuccess)
+        err = make_tmap_bf16_2d(&tm_hl, a.ws + a.L.H, (uint64_t)(a.k + 1) * a.T, 2 * (uint64_t)a.I,
+                                (uint64_t)a.I * 4, kBK, kTmBoxL);
     if (err != cudaSuccess) return err;
-    ffn_kernel<true><<<a.num_sms, kThreads, smem_bytes<true>(), st>>>(tm_h, tm_h, make_params(a, false));
+    ffn_tm_kernel<true><<<a.num_sms, kTmThreads, tm_smem_bytes<true>(), st>>>(tm_h, tm_hl, tm_h, tm_hl,
+                                                                             make_tm_params(a, false));
     *launches += 1;
     return cudaGetLastError();
 }
+
+}  // namespace moe
+
+namespace moe {
+cudaError_t launch_combine_rows(int T, int d, int k, const float* Y, const int32_t* pos, uint16_t* y, cudaStream_t st,
+                                unsigned long long* launches) {
+    const size_t n = (size_t)T * (d / 4);
+    const int blocks = (int)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
+    combine_rows_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(Y), pos, reinterpret_cast<uint2*>(y), T,
+                                                d / 4, k);
+    *launches += 1;
+    return cudaGetLastError();
+}
+}  // namespace moe
+
+// ======================================================================================
+// combine of the decode kernels' fp32 token-order sum (and of large prefill chunks):
+// y = bf16(sum), and the sum is left at zero (the one-launch decode kernel relies on that)
+// ======================================================================================
+namespace moe {
+namespace {
+__global__ void combine_kernel(float4* __restrict__ acc, uint2* __restrict__ y, size_t n4) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 v = acc[i];
+        y[i] = make_uint2((uint32_t)f32_to_bf16_rn(v.x) | ((uint32_t)f32_to_bf16_rn(v.y) << 16),
+                          (uint32_t)f32_to_bf16_rn(v.z) | ((uint32_t)f32_to_bf16_rn(v.w) << 16));
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+}  // namespace
 
 cudaError_t launch_combine(int T, int d, const float* acc, uint16_t* y, cudaStream_t st, unsigned long long* launches) {
     const size_t n4 = (size_t)T * d / 4;
     const int blocks = (int)((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096);
-    combine_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<float4*>(const_cast<float*>(acc)), reinterpret_cast<uint2*>(y), n4);
+    combine_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<float4*>(const_cast<float*>(acc)), reinterpret_cast<uint2*>(y),
+                                           n4);
     *launches += 1;
     return cudaGetLastError();
 }
-
 }  // namespace moe

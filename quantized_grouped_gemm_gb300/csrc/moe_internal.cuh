@@ -56,10 +56,6 @@ struct WsLayout {
     size_t gu_num;      // int32
     size_t dn_tiles;    // int4 [max_dn]
     size_t dn_num;      // int32
-    size_t gu_small;    // int4 [n_small * I/128]: tiles of at most kSmallRows token rows (warp-MMA kernel)
-    size_t gu_small_num;
-    size_t dn_small;    // int4 [n_small * d/256]
-    size_t dn_small_num;
     size_t xs;          // bf16 [k*T][d] rows in expert-group order
     size_t H;           // bf16 [(k+1)*T][2*I] (hi | lo)
     size_t acc;         // fp32 [T][d] token-order sum (decode kernels)
@@ -73,21 +69,18 @@ struct WsLayout {
 
 constexpr int kRouteBlockTokens = 32;   // tokens per routing block (one warp, one bitmask)
 constexpr int kMaxN = 128;              // max token rows of a GEMM tile (MMA M)
-#ifndef MOE_FFN_TMEM
-#define MOE_FFN_TMEM 1                  // grouped FFN with the dequantised weights in TMEM (one tile list)
-#endif
 #ifndef MOE_GU_ROWS
 #define MOE_GU_ROWS 128                 // token rows of a gate/up block (TMEM-operand FFN)
 #endif
 #ifndef MOE_DN_ROWS
 #define MOE_DN_ROWS 128                 // token rows of a down-projection block (TMEM-operand FFN)
 #endif
-constexpr int kSmallRows = 32;          // token blocks up to this size run on the warp-MMA kernel
 constexpr int kDecodeMaxT = 8;          // largest T the decode (GEMV) kernels take
 // token rows of a gate/up and of a down-projection block (smaller blocks were measured slower
 // at 4096 tokens: per-token dequant and MMA issue outweigh the overlap they allow)
-constexpr int kGuRows = MOE_FFN_TMEM ? MOE_GU_ROWS : kMaxN;
-constexpr int kDnRows = MOE_FFN_TMEM ? MOE_DN_ROWS : kMaxN;
+constexpr int kGuRows = MOE_GU_ROWS;
+constexpr int kDnRows = MOE_DN_ROWS;
+static_assert(kGuRows % 16 == 0 && kGuRows <= kMaxN && kDnRows % 16 == 0 && kDnRows <= kMaxN, "block rows");
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -135,13 +128,6 @@ inline WsLayout ws_layout(const moe_shape& s) {
     L.gu_num = o; o = align_up(o + 16, 256);
     L.dn_tiles = o; o = align_up(o + (size_t)L.max_dn * 16, 256);
     L.dn_num = o; o = align_up(o + 16, 256);
-    // small lists: one block per routed expert with <= kSmallRows rows, and up to 32 blocks of
-    // the shared expert (T <= 1024)
-    const size_t nsmall = (size_t)E + (T <= 1024 ? (T + kSmallRows - 1) / kSmallRows : 0);
-    L.gu_small = o; o = align_up(o + nsmall * (I / kTileRows) * 16, 256);
-    L.gu_small_num = o; o = align_up(o + 16, 256);
-    L.dn_small = o; o = align_up(o + nsmall * (d / 256) * 16, 256);
-    L.dn_small_num = o; o = align_up(o + 16, 256);
     L.xs = o; o = align_up(o + (size_t)k * T * d * 2 + 256 * d * 2, 1024);
     L.H = o; o = align_up(o + (size_t)(k + 1) * T * 2 * I * 2 + 256 * 2 * I * 2, 1024);
     L.acc = o; o = align_up(o + (size_t)T * d * 4, 256);
@@ -607,10 +593,6 @@ struct FfnArgs {
 
 cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_route_decode(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);
-cudaError_t launch_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
-cudaError_t launch_down(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
-cudaError_t launch_gate_up_small(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
-cudaError_t launch_down_small(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_combine(int T, int d, const float* acc, uint16_t* y, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_decode_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_decode_down(const FfnArgs& a, uint16_t* y, cudaStream_t st, unsigned long long* launches);

@@ -15,10 +15,10 @@
 //                      of the fixed-order logits; only those are recomputed exactly (CUDA
 //                      cores, fixed fp32 order) and ranked; weights; per-block counts.
 //   route_scan         one CTA: per-block bases, counts, offsets, the exported block map
-//                      and the GEMM tile lists (expert, first row, rows, 128-row M tile).
+//                      and the GEMM tile lists (expert, first row, rows, weight tile).
 //   route_scatter      one CTA per (block, slot): stable group positions (rank of the token among
 //                      the block's tokens routed to the same expert, from a bitmask), perm /
-//                      pos, the gathered rows xs, and zeroing of the fp32 token-order sum.
+//                      pos and the gathered rows xs.
 // Decode (one launch): route_decode -- a warp per expert logit, the last CTA to finish
 // does top-8 and the metadata for the few tokens.
 #include "moe_internal.cuh"
@@ -53,43 +53,6 @@ __device__ __forceinline__ float warp_pinned_logit(const uint16_t* xrow, const u
     for (int m = 16; m >= 1; m >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, m);
     if (bias_e) p = p + *bias_e;
     return p;
-}
-
-// Same value with the token row already in registers (xv[i] = columns 256 i + 8 lane .. +7,
-// NI = d / 256 <= 8) and all loads of the expert row issued before the arithmetic.
-template <int NI>
-__device__ __forceinline__ float warp_pinned_logit_regs(const uint4 (&xv)[8], const uint16_t* wrow, int lane,
-                                                        const float* bias_e) {
-    uint4 wv[NI];
-#pragma unroll
-    for (int i = 0; i < NI; ++i) wv[i] = ld_nc_v4(wrow + 256 * i + 8 * lane);
-    float p = 0.f;
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-        p = fmaf(bf16lo(xv[i].x), bf16lo(wv[i].x), p);
-        p = fmaf(bf16hi(xv[i].x), bf16hi(wv[i].x), p);
-        p = fmaf(bf16lo(xv[i].y), bf16lo(wv[i].y), p);
-        p = fmaf(bf16hi(xv[i].y), bf16hi(wv[i].y), p);
-        p = fmaf(bf16lo(xv[i].z), bf16lo(wv[i].z), p);
-        p = fmaf(bf16hi(xv[i].z), bf16hi(wv[i].z), p);
-        p = fmaf(bf16lo(xv[i].w), bf16lo(wv[i].w), p);
-        p = fmaf(bf16hi(xv[i].w), bf16hi(wv[i].w), p);
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, m);
-    if (bias_e) p = p + *bias_e;
-    return p;
-}
-
-__device__ __forceinline__ float pinned_logit_any(const uint4 (&xv)[8], const uint16_t* xrow, const uint16_t* wrow,
-                                                  int d, int lane, const float* bias_e) {
-    switch (d / 256) {
-        case 1: return warp_pinned_logit_regs<1>(xv, wrow, lane, bias_e);
-        case 2: return warp_pinned_logit_regs<2>(xv, wrow, lane, bias_e);
-        case 4: return warp_pinned_logit_regs<4>(xv, wrow, lane, bias_e);
-        case 8: return warp_pinned_logit_regs<8>(xv, wrow, lane, bias_e);
-        default: return warp_pinned_logit(xrow, wrow, d, lane, bias_e);
-    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -470,7 +433,7 @@ __device__ __forceinline__ int block_exclusive_scan256(int v, int* s_tmp) {
 
 __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     __shared__ int s_tmp[8];
-    __shared__ int s_tot[4];   // [0] block-map tiles, [1] large GEMM blocks, [2] small GEMM blocks
+    __shared__ int s_tot[4];   // [0] block-map tiles, [1] gate/up blocks, [2] down blocks
     __shared__ int s_part[4][256];
     __shared__ int s_off[256];
     const int E = 256;
@@ -548,30 +511,18 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     // tile innermost, so the CTAs that run at the same time share the block's activation rows
     // in L2).  The shared expert (expert index E) comes first and covers token rows 0..T-1.
     const int MTgu = a.I / kTileRows, MTdn = a.d / 256;   // 128 gate+up row pairs; 256-row down tiles
-    // experts with at most kSmallRows rows go to the small-tile lists as one block
-    // (the TMEM-operand FFN takes every block size from the main lists)
-    const bool small = !MOE_FFN_TMEM && run > 0 && run <= kSmallRows;
-    const int nn = small ? 0 : (run + kGuRows - 1) / kGuRows;
-    const int nd = small ? 0 : (run + kDnRows - 1) / kDnRows;
-    // the shared expert runs in kSmallRows-row blocks on the warp-MMA kernel when the chunk is
-    // small enough that the routed groups mostly are (T <= 1024: 8T/E <= 32 rows on average)
-    const bool sh_small = !MOE_FFN_TMEM && a.T <= 1024;
-    const int nsh = sh_small ? 0 : (a.T + kGuRows - 1) / kGuRows;
-    const int nshd = sh_small ? 0 : (a.T + kDnRows - 1) / kDnRows;
-    const int nshs = sh_small ? (a.T + kSmallRows - 1) / kSmallRows : 0;
+    const int nn = (run + kGuRows - 1) / kGuRows;
+    const int nd = (run + kDnRows - 1) / kDnRows;
+    const int nsh = (a.T + kGuRows - 1) / kGuRows;
+    const int nshd = (a.T + kDnRows - 1) / kDnRows;
     const int nbase = block_exclusive_scan256(nn, s_tmp);
     if (e == E - 1) s_tot[1] = nbase + nn;
     named_bar_sync(1, 256);
     const int dbase = block_exclusive_scan256(nd, s_tmp);
-    if (e == E - 1) s_tot[3] = dbase + nd;
-    named_bar_sync(1, 256);
-    const int sbase = block_exclusive_scan256(small ? 1 : 0, s_tmp);
-    if (e == E - 1) s_tot[2] = sbase + (small ? 1 : 0);
+    if (e == E - 1) s_tot[2] = dbase + nd;
     named_bar_sync(1, 256);
     int4* gu = reinterpret_cast<int4*>(a.ws + a.L.gu_tiles);
     int4* dn = reinterpret_cast<int4*>(a.ws + a.L.dn_tiles);
-    int4* gus = reinterpret_cast<int4*>(a.ws + a.L.gu_small);
-    int4* dns = reinterpret_cast<int4*>(a.ws + a.L.dn_small);
     // nb near-equal blocks of `rows` rows from r0; block i goes to list slot base + i
     auto split = [&](int4* list, int mt, int base, int ex, int r0, int rows, int nb) {
         const int q = rows / nb, rem = rows % nb;
@@ -581,13 +532,8 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
             r0 += n;
         }
     };
-    auto emit_small = [&](int slot, int ex, int r0, int rows) {
-        for (int m = 0; m < MTgu; ++m) gus[(size_t)slot * MTgu + m] = make_int4(ex, r0, rows, m);
-        for (int m = 0; m < MTdn; ++m) dns[(size_t)slot * MTdn + m] = make_int4(ex, r0, rows, m);
-    };
     if (nn > 0) split(gu, MTgu, nsh + nbase, e, off, run, nn);
     if (nd > 0) split(dn, MTdn, nshd + dbase, e, off, run, nd);
-    if (small) emit_small(nshs + sbase, e, off, run);
     // shared expert token blocks (one thread each)
     for (int i = e; i < nsh; i += E) {
         const int q = a.T / nsh, rem = a.T % nsh;
@@ -597,14 +543,10 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
         const int q = a.T / nshd, rem = a.T % nshd;
         split(dn, MTdn, i, E, i * q + min(i, rem), q + (i < rem ? 1 : 0), 1);
     }
-    for (int i = e; i < nshs; i += E) emit_small(i, E, i * kSmallRows, min(kSmallRows, a.T - i * kSmallRows));
     if (e == 0) {
         *a.num_tiles = s_tot[0];
-        const int total_s = nshs + s_tot[2];
         *reinterpret_cast<int32_t*>(a.ws + a.L.gu_num) = (nsh + s_tot[1]) * MTgu;
-        *reinterpret_cast<int32_t*>(a.ws + a.L.dn_num) = (nshd + s_tot[3]) * MTdn;
-        *reinterpret_cast<int32_t*>(a.ws + a.L.gu_small_num) = total_s * MTgu;
-        *reinterpret_cast<int32_t*>(a.ws + a.L.dn_small_num) = total_s * MTdn;
+        *reinterpret_cast<int32_t*>(a.ws + a.L.dn_num) = (nshd + s_tot[2]) * MTdn;
     }
 }
 
