@@ -23,10 +23,10 @@
 //            half and its lo half: for N <= 32 as one B operand of 2N rows (hi rows, then lo
 //            rows; y = D[n] + D[N + n]), else as two MMAs per K step into the same D; weight * y
 //            (fp32) leaves the chunk in one of two ways, chosen by whether the weighted rows fit
-//            well inside L2: stored into Y [d/256][(k+1)T][256] at the row index of h (the rows
-//            of a 32-token chunk are one contiguous block of a 256-column tile: one TMA bulk
+//            well inside L2: stored into Y [d/128][(k+1)T][128] at the row index of h (the rows
+//            of a 32-token chunk are one contiguous block of a 128-column tile: one TMA bulk
 //            copy; plain stores, no atomics), or added into the fp32 token-order sum with one
-//            1 KB bulk reduce-add per token.
+//            512-byte bulk reduce-add per token and matrix.
 // combine_rows sums each token's k routed rows and its shared row of Y in a fixed order.
 // Warp roles (28 warps):
 //   0-15  dequant, two sets of 8 warps taking alternate K blocks: warp w owns row 32 (w & 3) +
@@ -43,10 +43,15 @@
 //         tcgen05.mma about every 54 cycles, while the tensor core finishes a 128 x N x 16 MMA
 //         with A in TMEM in N / 2 cycles: two issuers double the rate for small N); warp 26
 //         owns the TMEM allocation
-// TMEM (512 columns): A ring of 4 slots x 64 columns at columns 0..255 (slot s, matrix m, K step
-// ks at 64 s + 32 m + 8 ks); accumulators in two D slots of 128 columns at 256 and 384.  A tile
-// whose two accumulators fit in 128 columns (gate/up N <= 64; down N <= 64) takes one slot, so the next tile's MMAs run while the epilogue drains it; a larger tile
-// takes both (D_m in its own slot).  MMA threads and epilogue walk the same slot sequence.
+// TMEM (512 columns): an A ring of slots of 64 columns from column 0 (slot s, matrix m, K step ks
+// at 64 s + 32 m + 8 ks), then accumulator slots of 128 columns.
+//   gate/up  4 A slots, 2 D slots: a tile whose two accumulators fit in 128 columns (N <= 64)
+//            takes one slot, so the next tile's MMAs run while the epilogue drains it; a larger
+//            tile takes both (D_m in its own slot).
+//   down     2 A slots (its MMAs are the slower stage), 3 D slots: matrix m of the t-th tile is use
+//            j = 2t + m of the slot ring (slot j % 3); the epilogue drains matrix 0 and frees its
+//            slot before matrix 1, so a matrix's next slot is free before its MMAs need it.
+// MMA threads and epilogue walk the same slot sequence.
 // Each MMA thread commits once per K block to a ring of "K block done" barriers (two arrivals);
 // the dequant sets (A slot reuse) and the token-row producer (token-row slot reuse) wait on it.
 // One "ready" barrier per K block collects the dequant set's warps and the token-row bytes, so
@@ -67,7 +72,6 @@ constexpr int kTmXWarp = kTmCodeWarp + 1;
 constexpr int kTmMmaWarp = kTmXWarp + 1;                 // two MMA warps
 constexpr int kTmThreads = (kTmMmaWarp + 2) * 32;
 
-constexpr int kTmA = 4;                       // A ring slots (TMEM)
 constexpr int kTmBox = 16;                    // token rows per small TMA box
 constexpr int kTmBoxL = 64;                   // token rows per large TMA box
 constexpr int kTmKD = 8;                      // "K block done" barriers
@@ -75,12 +79,18 @@ constexpr int kTmXBytes = kMaxN * 128;        // token rows of one K block: 128 
 
 template <bool kDown>
 struct TmCfg {
-    static constexpr int RX = kDown ? 3 : 8;                 // token-row ring slots
+    // TMEM: A ring of A slots x 64 columns from column 0, then NDS accumulator slots of 128
+    // columns from column DCOL0
+    static constexpr int A = kDown ? 2 : 4;
+    static constexpr int NDS = kDown ? 3 : 2;
+    static constexpr uint32_t DCOL0 = 64u * A;
+    static_assert(DCOL0 + 128u * NDS == 512u, "TMEM columns");
+    static constexpr int RX = kDown ? 4 : 8;                 // token-row ring slots
     static constexpr int RC = kDown ? 6 : 8;                 // packed-code ring slots
     static constexpr int PARTS = kDown ? 2 : 1;              // hi, lo halves of h
     static constexpr int XS = PARTS * kTmXBytes;             // bytes of a token-row slot
-    // staging of 32 tokens: gate/up bf16 [32][hi 128 | lo 128]; down two buffers of fp32 [32][256]
-    static constexpr int STAGE = kDown ? 2 * 32 * 1024 : 32 * 512;
+    // staging of 32 tokens: gate/up bf16 [32][hi 128 | lo 128]; down two buffers of fp32 [32][128]
+    static constexpr int STAGE = kDown ? 2 * 32 * 512 : 32 * 512;
     static constexpr int x_off = 0;
     static constexpr int c_off = x_off + RX * XS;
     static constexpr int stage_off = c_off + RC * kChunkPairBytes;
@@ -90,7 +100,7 @@ struct TmCfg {
 
 struct TmBars {
     uint64_t c_full[8], c_empty[8], ready[kTmKD], kb_done[kTmKD];
-    uint64_t d_full[2], d_empty[2], drain[2];
+    uint64_t d_full[3], d_empty[3], drain[2];
     uint32_t tmem_slot;
     int abort;
 };
@@ -224,7 +234,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         for (int i = 0; i < C::RC; ++i) { mbar_init(&b->c_full[i], 1); mbar_init(&b->c_empty[i], kTmDeqSet); }
         // ready: the 8 dequant warps of a K block's set + the token-row producer (with its bytes)
         for (int i = 0; i < kTmKD; ++i) { mbar_init(&b->ready[i], kTmDeqSet + 1); mbar_init(&b->kb_done[i], 2); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&b->d_full[i], 2); mbar_init(&b->d_empty[i], kTmEpiWarps); }
+        // gate/up: both MMA threads commit to a tile's slot(s); down: slot = one matrix's accumulator
+        for (int i = 0; i < C::NDS; ++i) { mbar_init(&b->d_full[i], kDown ? 1 : 2); mbar_init(&b->d_empty[i], kTmEpiWarps); }
         mbar_init(&b->drain[0], 1);
         mbar_init(&b->drain[1], 1);
         b->abort = 0;
@@ -303,24 +314,35 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     } else if (warp >= kTmMmaWarp) {
         if (lane == 0) {
             const int m = warp - kTmMmaWarp;   // this thread's accumulator D_m and A matrix m
-            uint32_t it = 0, tcount = 0, sc = 0, use[2] = {0, 0};
+            uint32_t it = 0, tcount = 0, sc = 0, use[3] = {0, 0, 0};
             bool ok = true;
             const uint64_t xdesc0 = sw128_desc(smem_u32(xring));   // start address advances 16 B per unit
             for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x, ++tcount) {
                 const int N = tile_n(p.tiles[tile].z);
                 const bool stacked = kDown && down_stacked(N);   // hi and lo rows as one B operand of 2N rows
                 const uint32_t idesc = idesc_bf16_f32(128, stacked ? 2 * N : N);
+                // gate/up: one or two slots per tile (d_slots); down: use j = 2 tcount + m of the
+                // slot ring, slot j % 3, phase j / 3 (matrices of consecutive tiles take turns, so a
+                // matrix's next slot was drained one matrix earlier)
                 const DSlots ds = d_slots(sc, N, kDown);
-                if (!mbar_wait(&b->d_empty[ds.s0], (use[ds.s0] & 1) ^ 1, abort) ||
-                    (ds.two && !mbar_wait(&b->d_empty[ds.s1], (use[ds.s1] & 1) ^ 1, abort))) { ok = false; break; }
+                const uint32_t dj = 2 * tcount + m;
+                const int dsl = kDown ? (int)(dj % 3) : 0;
+                if (kDown) {
+                    if (!mbar_wait(&b->d_empty[dsl], ((dj / 3) & 1) ^ 1, abort)) { ok = false; break; }
+                } else if (!mbar_wait(&b->d_empty[ds.s0], (use[ds.s0] & 1) ^ 1, abort) ||
+                           (ds.two && !mbar_wait(&b->d_empty[ds.s1], (use[ds.s1] & 1) ^ 1, abort))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
+                const uint32_t dm = tmem + (kDown ? C::DCOL0 + 128u * dsl : (m ? ds.col1 : ds.col0));
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int as = it % kTmA, xs = it % C::RX;
+                    const int as = it % C::A, xs = it % C::RX;
                     if (!mbar_wait(&b->ready[it % kTmKD], (it / kTmKD) & 1, abort)) { ok = false; break; }
                     tc_fence_after();
                     if (m == 0) TM_TRACE(TT_MW, it);
                     const uint64_t xd = xdesc0 + (uint64_t)((xs * C::XS) >> 4);
-                    const uint32_t a0 = tmem + 64u * as + 32u * m, dm = tmem + (m ? ds.col1 : ds.col0);
+                    const uint32_t a0 = tmem + 64u * as + 32u * m;
                     const int parts = stacked ? 1 : C::PARTS;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
@@ -332,11 +354,15 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                     if (m == 0) TM_TRACE(TT_MD, it);
                 }
                 if (!ok) break;
-                tc_commit(&b->d_full[ds.s0]);
-                if (ds.two) tc_commit(&b->d_full[ds.s1]);
-                use[ds.s0]++;
-                if (ds.two) use[ds.s1]++;
-                sc += ds.two ? 2 : 1;
+                if (kDown) {
+                    tc_commit(&b->d_full[dsl]);
+                } else {
+                    tc_commit(&b->d_full[ds.s0]);
+                    if (ds.two) tc_commit(&b->d_full[ds.s1]);
+                    use[ds.s0]++;
+                    if (ds.two) use[ds.s1]++;
+                    sc += ds.two ? 2 : 1;
+                }
             }
             if (!ok) tm_abort(abort, p.status);
             tc_commit(&b->drain[m]);
@@ -356,10 +382,10 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             const bool denorm = __all_sync(0xffffffffu, (p.tiles[tile].x < p.E ? mode_r : mode_s) == kScaleDenorm);
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 if ((int)(it & 1) != set) continue;
-                const int cs = it % C::RC, as = it % kTmA;
-                const uint32_t g = it - kTmA;   // the K block that last used this A slot
+                const int cs = it % C::RC, as = it % C::A;
+                const uint32_t g = it - C::A;   // the K block that last used this A slot
                 const bool got = mbar_wait(&b->c_full[cs], (it / C::RC) & 1, abort) &&
-                                 (it < (uint32_t)kTmA || mbar_wait(&b->kb_done[g % kTmKD], (g / kTmKD) & 1, abort));
+                                 (it < (uint32_t)C::A || mbar_wait(&b->kb_done[g % kTmKD], (g / kTmKD) & 1, abort));
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 if (threadIdx.x == 0) TM_TRACE(TT_DW, it);
                 const uint8_t* ch = cring + cs * kChunkPairBytes;
@@ -395,7 +421,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         int* s_tok = reinterpret_cast<int*>(smem + C::tab_off + 512);
         const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
         const size_t yrows = (size_t)(p.k + 1) * p.T;
-        uint32_t tcount = 0, chunk = 0, sc = 0, use[2] = {0, 0};
+        uint32_t tcount = 0, chunk = 0, sc = 0, use[3] = {0, 0, 0};
         bool ok = true;
         for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x, ++tcount) {
             const int4 t = p.tiles[tile];
@@ -406,19 +432,19 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                 s_w[et] = e < p.E ? p.topk_w[asg] : 1.0f;
                 s_tok[et] = e < p.E ? asg / p.k : row0 + et;
             }
-            const DSlots ds = d_slots(sc, N, kDown);
-            if (et == 0 && (!mbar_wait(&b->d_full[ds.s0], use[ds.s0] & 1, abort) ||
-                            (ds.two && !mbar_wait(&b->d_full[ds.s1], use[ds.s1] & 1, abort))))
-                tm_abort(abort, p.status);
-            named_bar_sync(2, kTmEpiThreads);
-            if (*abort) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t td0 = tlane + ds.col0, td1 = tlane + ds.col1;   // this lane quadrant's D_0, D_1
-            if (et == 0) TM_TRACE(TT_ET, tcount);
-            for (int c0 = 0; c0 < N; c0 += 32, ++chunk) {
-                const int c = c0 + 16 * half;          // this warp's 16 tokens: c .. c+15
-                const bool last = c0 + 32 >= N;
-                if (!kDown) {
+            if (!kDown) {
+                const DSlots ds = d_slots(sc, N, false);
+                if (et == 0 && (!mbar_wait(&b->d_full[ds.s0], use[ds.s0] & 1, abort) ||
+                                (ds.two && !mbar_wait(&b->d_full[ds.s1], use[ds.s1] & 1, abort))))
+                    tm_abort(abort, p.status);
+                named_bar_sync(2, kTmEpiThreads);
+                if (*abort) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t td0 = tlane + ds.col0, td1 = tlane + ds.col1;   // this lane quadrant's D_0, D_1
+                if (et == 0) TM_TRACE(TT_ET, tcount);
+                for (int c0 = 0; c0 < N; c0 += 32) {
+                    const int c = c0 + 16 * half;          // this warp's 16 tokens: c .. c+15
+                    const bool last = c0 + 32 >= N;
                     uint16_t* st = reinterpret_cast<uint16_t*>(stage);   // [32][hi 128 | lo 128]
                     uint32_t G[16], U[16];
                     if (c < N) {
@@ -456,64 +482,75 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                         }
                     }
                     named_bar_sync(2, kTmEpiThreads);
-                } else {
-                    // two staging buffers, alternate chunks: a chunk's bulk copy reads one while
-                    // the next chunk is written into the other
-                    float* st = reinterpret_cast<float*>(stage) + (chunk & 1) * (32 * 256);   // [32][256]
-                    if (c < N) {
-                        const bool stacked = down_stacked(N);   // the lo half's products sit N columns further
-#pragma unroll
-                        for (int m = 0; m < 2; ++m) {
-                            uint32_t R[16], L[16];
-                            const uint32_t tdm = m ? td1 : td0;
-                            tmem_ld16(tdm + c, R);
-                            if (stacked) tmem_ld16(tdm + N + c, L);
+                }
+                use[ds.s0]++;
+                if (ds.two) use[ds.s1]++;
+                sc += ds.two ? 2 : 1;
+            } else {
+                // down: matrix 0 (output rows 256 wt ..) is drained and its slot released before
+                // matrix 1, so the next tile's MMAs into matrix 0 start half an epilogue earlier
+                if (et == 0) TM_TRACE(TT_ET, tcount);
+                const bool stacked = down_stacked(N);   // the lo half's products sit N columns further
+                for (int m = 0; m < 2; ++m) {
+                    const uint32_t dj = 2 * tcount + m;   // use j of the slot ring: slot j % 3, phase j / 3
+                    const int dsl = (int)(dj % 3);
+                    if (et == 0 && !mbar_wait(&b->d_full[dsl], (dj / 3) & 1, abort)) tm_abort(abort, p.status);
+                    named_bar_sync(2, kTmEpiThreads);   // (also: the weight / token tables are written)
+                    if (*abort) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t td = tlane + C::DCOL0 + 128u * dsl;
+                    for (int c0 = 0; c0 < N; c0 += 32, ++chunk) {
+                        const int c = c0 + 16 * half;          // this warp's 16 tokens: c .. c+15
+                        const bool last = c0 + 32 >= N;
+                        // two staging buffers, alternate chunks: a chunk's bulk operations read one
+                        // while the next chunk is written into the other
+                        float* st = reinterpret_cast<float*>(stage) + (chunk & 1) * (32 * 128);   // [32][128]
+                        uint32_t R[16], L[16];
+                        if (c < N) {
+                            tmem_ld16(td + c, R);
+                            if (stacked) tmem_ld16(td + N + c, L);
                             tmem_ld_wait();
+                        }
+                        if (last) {   // this accumulator is no longer read: its slot is free
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&b->d_empty[dsl]);
+                        }
+                        if (c < N) {
 #pragma unroll
                             for (int u = 0; u < 16; ++u) {
                                 const float w = c + u < rows ? s_w[c + u] : 0.0f;
                                 const float y = __uint_as_float(R[u]) + (stacked ? __uint_as_float(L[u]) : 0.0f);
-                                st[(16 * half + u) * 256 + 128 * m + r] = w * y;
+                                st[(16 * half + u) * 128 + r] = w * y;
                             }
                         }
-                    }
-                    if (last) {   // D is no longer read: the next tile's MMAs may start
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) {
-                            mbar_arrive(&b->d_empty[ds.s0]);
-                            if (ds.two) mbar_arrive(&b->d_empty[ds.s1]);
+                        fence_proxy_async_smem();
+                        named_bar_sync(2, kTmEpiThreads);
+                        const int nv = rows - c0 < 32 ? rows - c0 : 32;   // rows of this chunk
+                        if (p.rows_out) {
+                            if (et == 0) {
+                                bulk_s2g(p.Y + ((size_t)(2 * wt + m) * yrows + orow0 + c0) * 128, st, (uint32_t)nv * 512);
+                                bulk_commit();
+                                bulk_wait_read1();   // the previous chunk (the other buffer) has been read
+                            }
+                        } else if (lane < 4) {
+                            // token n = (epilogue warp) + 8 lane: its 512-byte row piece added into
+                            // acc; the issues are spread over the eight warps
+                            const int n = (warp - kTmEpiWarp0) + 8 * lane;
+                            if (n < nv) {
+                                bulk_reduce_add_f32(p.acc + (size_t)s_tok[c0 + n] * p.d + (size_t)wt * 256 + 128 * m,
+                                                    st + n * 128, 512);
+                                bulk_commit();
+                                bulk_wait_read1();   // this lane's previous chunk has been read
+                            } else {
+                                bulk_wait_read0();
+                            }
                         }
+                        named_bar_sync(2, kTmEpiThreads);
                     }
-                    fence_proxy_async_smem();
-                    named_bar_sync(2, kTmEpiThreads);
-                    const int nv = rows - c0 < 32 ? rows - c0 : 32;   // rows of this chunk
-                    if (p.rows_out) {
-                        if (et == 0) {
-                            bulk_s2g(p.Y + ((size_t)wt * yrows + orow0 + c0) * 256, st, (uint32_t)nv * 1024);
-                            bulk_commit();
-                            bulk_wait_read1();   // the previous chunk (the other buffer) has been read
-                        }
-                    } else if (lane < 4) {
-                        // token n = (epilogue warp) + 8 lane: its 1 KB row added into acc; the
-                        // issues are spread over the eight warps
-                        const int n = (warp - kTmEpiWarp0) + 8 * lane;
-                        if (n < nv) {
-                            bulk_reduce_add_f32(p.acc + (size_t)s_tok[c0 + n] * p.d + (size_t)wt * 256, st + n * 256,
-                                                1024);
-                            bulk_commit();
-                            bulk_wait_read1();   // this lane's previous chunk has been read
-                        } else {
-                            bulk_wait_read0();
-                        }
-                    }
-                    named_bar_sync(2, kTmEpiThreads);
                 }
             }
             if (et == 0) TM_TRACE(TT_ED, tcount);
-            use[ds.s0]++;
-            if (ds.two) use[ds.s1]++;
-            sc += ds.two ? 2 : 1;
         }
         if (!ok && lane == 0) tm_abort(abort, p.status);
         if (kDown && (et == 0 || lane < 4)) bulk_wait0();   // every bulk copy / reduce-add has completed
@@ -526,19 +563,19 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 }
 
 // y[t] = bf16( sum_j Y[pos[t k + j]] + Y[k T + t] ), j = 0..k-1 in order, then the shared row;
-// Y is [d/256][(k+1)T][256]; one thread per 4 columns of a token (16-byte loads, 8-byte store).
+// Y is [d/128][(k+1)T][128]; one thread per 4 columns of a token (16-byte loads, 8-byte store).
 __global__ void combine_rows_kernel(const float4* __restrict__ Y, const int32_t* __restrict__ pos,
                                     uint2* __restrict__ y, int T, int d4, int k) {
-    const size_t n = (size_t)T * d4, tile4 = (size_t)(k + 1) * T * 64;   // float4s of a 256-column tile
+    const size_t n = (size_t)T * d4, tile4 = (size_t)(k + 1) * T * 32;   // float4s of a 128-column tile
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / d4), c = (int)(i % d4);
-        const float4* Yc = Y + (size_t)(c >> 6) * tile4 + (c & 63);
+        const float4* Yc = Y + (size_t)(c >> 5) * tile4 + (c & 31);
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
-            const float4 v = __ldcs(Yc + (size_t)pos[(size_t)t * k + j] * 64);
+            const float4 v = __ldcs(Yc + (size_t)pos[(size_t)t * k + j] * 32);
             s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
         }
-        const float4 v = __ldcs(Yc + ((size_t)k * T + t) * 64);
+        const float4 v = __ldcs(Yc + ((size_t)k * T + t) * 32);
         s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
         y[i] = make_uint2((uint32_t)f32_to_bf16_rn(s.x) | ((uint32_t)f32_to_bf16_rn(s.y) << 16),
                           (uint32_t)f32_to_bf16_rn(s.z) | ((uint32_t)f32_to_bf16_rn(s.w) << 16));
