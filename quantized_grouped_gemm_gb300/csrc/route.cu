@@ -182,8 +182,8 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ---------------------------------------------------------------------------------------
-// route_certify_topk: grid = ceil(T/32) blocks, 512 threads (warp w: tokens w, w + 16).
-// For each token, with l~[e] the tensor-core logit (sum of the K slices, + bias) and
+// route_certify_topk (the bound): for each token, with l~[e] the tensor-core logit (sum of the
+// K slices, + bias) and
 //   delta[e] = c * ||x_t|| * ||W_r[e]||,  c = 2 * ((d + 4 + 35) * 2^-23)  (+ a bias term),
 // which bounds |l~[e] - l[e]| for the fixed-order logit l (any fp32 summation of d exact
 // products errs by at most ~d*2^-23 * sum|x w| <= d*2^-23 ||x|| ||w||; the fixed order by
@@ -253,16 +253,23 @@ __device__ __forceinline__ float key32_logit(uint32_t k) {
 }
 
 // ---------------------------------------------------------------------------------------
-// route_certify_topk: one warp per token, 16 tokens per CTA (two CTAs per 32-token block).
+// route_certify_topk: one warp per token, kCertTokens tokens per CTA.
 // From the tensor-core partial logits l~ and the bound delta of each expert it keeps the
 // candidates l~ + delta >= lo with lo = (8th largest l~) - max delta (at least eight experts
 // have an exact logit >= lo, so no other expert can be in the exact top-8), recomputes their
 // exact logits in the fixed order, two at a time, and takes the top-k among them.  More than
 // 32 candidates: all 256 are recomputed.  Per-block expert counts are added for the scan.
 // ---------------------------------------------------------------------------------------
-constexpr int kCertTokens = 16;
+#ifndef MOE_CERT_TOKENS
+#define MOE_CERT_TOKENS 8
+#endif
+// tokens (warps) per CTA: few, so that a small chunk still spreads over the SMs (each warp's
+// exact recomputation is a chain of L2 loads; 2, 4, 8 and 16 measured within 10 % of each
+// other at 512 tokens, 8 the fastest); divides the 32-token routing block
+constexpr int kCertTokens = MOE_CERT_TOKENS;
+static_assert(kRouteBlockTokens % kCertTokens == 0, "certify tokens per CTA");
 
-__global__ void __launch_bounds__(512) route_certify_topk(RouteArgs a, int KS) {
+__global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs a, int KS) {
     __shared__ uint32_t s_mask[256];
     __shared__ float s_all[kCertTokens][256];
     __shared__ int s_cand[kCertTokens][32];
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(512) route_certify_topk(RouteArgs a, int KS) {
     const float* part = reinterpret_cast<const float*>(a.ws + a.L.rpart);
     const float* wnorm = reinterpret_cast<const float*>(a.ws + a.L.wnorm);
     const float c = 2.0f * (float)(a.d + 4 + 35) * 1.1920928955078125e-7f;   // 2^-23
-    if (threadIdx.x < 256) s_mask[threadIdx.x] = 0;
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) s_mask[i] = 0;
     __syncthreads();
     if (tok < a.T) {
         const uint16_t* xrow = a.x + (size_t)tok * a.d;
@@ -403,10 +410,11 @@ __global__ void __launch_bounds__(512) route_certify_topk(RouteArgs a, int KS) {
         __syncwarp();
     }
     __syncthreads();
-    if (threadIdx.x < 256 && s_mask[threadIdx.x]) {   // per 32-token block counts (cleared by the scan)
-        int32_t* blk_counts = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
-        atomicAdd(&blk_counts[(size_t)(blockIdx.x / 2) * 256 + threadIdx.x], __popc(s_mask[threadIdx.x]));
-    }
+    // per 32-token block counts (cleared by the scan)
+    int32_t* blk_counts = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
+    const size_t blk = (size_t)blockIdx.x * kCertTokens / kRouteBlockTokens;
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+        if (s_mask[i]) atomicAdd(&blk_counts[blk * 256 + i], __popc(s_mask[i]));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -758,7 +766,7 @@ cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned l
     if (err != cudaSuccess) return err;
     router_wnorm<<<256 / 4, 128, 0, st>>>(a);
     router_tc<<<dim3((a.T + 127) / 128, KS), 192, kRtSmem, st>>>(tm_x, tm_w, a, KS);
-    route_certify_topk<<<(a.T + kCertTokens - 1) / kCertTokens, 512, 0, st>>>(a, KS);
+    route_certify_topk<<<(a.T + kCertTokens - 1) / kCertTokens, 32 * kCertTokens, 0, st>>>(a, KS);
     route_scan<<<1, 1024, 0, st>>>(a);
     route_scatter<<<dim3(nblk, a.k), 256, 0, st>>>(a);
     *launches += 5;
