@@ -343,12 +343,19 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                     if (m == 0) TM_TRACE(TT_MW, it);
                     const uint64_t xd = xdesc0 + (uint64_t)((xs * C::XS) >> 4);
                     const uint32_t a0 = tmem + 64u * as + 32u * m;
-                    const int parts = stacked ? 1 : C::PARTS;
+                    // both loops fully unrolled: the issuing thread's instruction count sets its pace
+                    if (C::PARTS == 1 || stacked) {
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        for (int part = 0; part < parts; ++part)
-                            tc_mma_bf16_ts(dm, a0 + 8u * ks, xd + (uint64_t)((part * kTmXBytes + ks * 32) >> 4), idesc,
-                                           (kb | ks | part) ? 1u : 0u);
+                        for (int ks = 0; ks < 4; ++ks)
+                            tc_mma_bf16_ts(dm, a0 + 8u * ks, xd + (uint64_t)(ks * 2), idesc, (kb | ks) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+                            for (int part = 0; part < C::PARTS; ++part)
+                                tc_mma_bf16_ts(dm, a0 + 8u * ks, xd + (uint64_t)((part * kTmXBytes + ks * 32) >> 4), idesc,
+                                               (kb | ks | part) ? 1u : 0u);
+                        }
                     }
                     tc_commit(&b->kb_done[it % kTmKD]);
                     if (m == 0) TM_TRACE(TT_MD, it);
