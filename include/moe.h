@@ -112,7 +112,12 @@ typedef struct moe_options {
     int tile_rows;          /* rows per exported block-map tile; default 32 */
     int decode_max_tokens;  /* T at or below this runs the decode (GEMV) kernels; default 1 */
     int decode_path;        /* MOE_DECODE_AUTO (default) or MOE_DECODE_GEMV */
-    int reserved[5];
+    int deterministic;      /* 0 (default): prefill sums each token's weighted rows in a fixed order
+                               when they fit well inside L2 ((k+1)*T*d*4 bytes <= 64 MB) and adds
+                               them into the fp32 sum with bulk reduce-adds otherwise (addition
+                               order not fixed); 1: always the fixed order, so repeated calls give
+                               identical bits (the rows then pass through HBM at large T) */
+    int reserved[4];
 } moe_options;
 
 /* Human-readable text for a return code. */

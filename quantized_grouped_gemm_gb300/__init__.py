@@ -48,9 +48,11 @@ def shape(T: int, d: int, E: int = 256, k: int = 8, I: int = 512, I_shared: Opti
 DECODE_AUTO, DECODE_GEMV = 0, 1
 
 
-def options(tile_rows: int = 32, decode_max_tokens: int = 1, decode_path: int = DECODE_AUTO) -> _lib.moe_options:
-    """decode_path: DECODE_AUTO (one fused launch per token when it fits) or DECODE_GEMV."""
-    return _lib.moe_options(tile_rows, decode_max_tokens, decode_path)
+def options(tile_rows: int = 32, decode_max_tokens: int = 1, decode_path: int = DECODE_AUTO,
+            deterministic: int = 0) -> _lib.moe_options:
+    """decode_path: DECODE_AUTO (one fused launch per token when it fits) or DECODE_GEMV.
+    deterministic: 1 = prefill sums each token's rows in a fixed order at every size."""
+    return _lib.moe_options(tile_rows, decode_max_tokens, decode_path, deterministic)
 
 
 def _p(t: Optional[torch.Tensor]):

@@ -44,7 +44,7 @@ class moe_routing(ctypes.Structure):
 
 class moe_options(ctypes.Structure):
     _fields_ = [("tile_rows", ctypes.c_int), ("decode_max_tokens", ctypes.c_int), ("decode_path", ctypes.c_int),
-                ("reserved", ctypes.c_int * 5)]
+                ("deterministic", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
 
 
 _SPS = ctypes.POINTER(moe_shape)

@@ -65,6 +65,7 @@ struct Opts {
     int tile_rows = 32;
     int decode_max_tokens = 1;
     int decode_path = MOE_DECODE_AUTO;
+    bool deterministic = false;
 };
 
 static int get_opts(const moe_options* o, Opts* out) {
@@ -76,6 +77,8 @@ static int get_opts(const moe_options* o, Opts* out) {
         r.decode_max_tokens = o->decode_max_tokens;
         if (o->decode_path != MOE_DECODE_AUTO && o->decode_path != MOE_DECODE_GEMV) return MOE_ERR_INVALID_ARG;
         r.decode_path = o->decode_path;
+        if (o->deterministic != 0 && o->deterministic != 1) return MOE_ERR_INVALID_ARG;
+        r.deterministic = o->deterministic == 1;
     }
     *out = r;
     return MOE_OK;
@@ -274,6 +277,7 @@ int moe_ffn_down(const moe_shape* s, const moe_routing* rt, const void* wr, cons
     int rc = ffn_common(s, nullptr, rt, wr, wsh, ws, ws_bytes, o, &op, false);
     if (rc != MOE_OK) return rc == 1 ? MOE_OK : rc;
     FfnArgs a = ffn_args(s, nullptr, rt, wr, wsh, ws);
+    a.rows_out = ffn_rows_output(s->T, s->d, s->k, op.deterministic);
     unsigned long long n = 0;
     cudaError_t e;
     if (is_decode(s, op)) {
@@ -305,7 +309,7 @@ int moe_combine(const moe_shape* s, const moe_routing* rt, void* ws, size_t ws_b
     uint8_t* w8 = static_cast<uint8_t*>(ws);
     unsigned long long n = 0;
     cudaError_t e;
-    if (!is_decode(s, op) && ffn_rows_output(s->T, s->d, s->k)) {
+    if (!is_decode(s, op) && ffn_rows_output(s->T, s->d, s->k, op.deterministic)) {
         // prefill: the down projection left weighted rows in Y; sum each token's rows
         if ((rc = check_routing(rt)) != MOE_OK) return rc;
         e = launch_combine_rows(s->T, s->d, s->k, reinterpret_cast<const float*>(w8 + L.Y), rt->pos_dev, y,

@@ -602,7 +602,7 @@ TmParams make_tm_params(const FfnArgs& a, bool gate_up) {
     p.H = reinterpret_cast<uint16_t*>(a.ws + a.L.H);
     p.Y = reinterpret_cast<float*>(a.ws + a.L.Y);
     p.acc = reinterpret_cast<float*>(a.ws + a.L.acc);
-    p.rows_out = ffn_rows_output(a.T, a.d, a.k) ? 1 : 0;
+    p.rows_out = a.rows_out ? 1 : 0;
     p.perm = a.perm;
     p.topk_w = a.topk_w;
     p.status = reinterpret_cast<int*>(a.ws + a.L.status);

@@ -92,7 +92,9 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 #define MOE_ROWS_OUT_MB 64
 #endif
 constexpr size_t kRowsOutputMaxBytes = (size_t)MOE_ROWS_OUT_MB << 20;
-inline bool ffn_rows_output(int T, int d, int k) { return (size_t)(k + 1) * T * d * 4 <= kRowsOutputMaxBytes; }
+inline bool ffn_rows_output(int T, int d, int k, bool deterministic) {
+    return deterministic || (size_t)(k + 1) * T * d * 4 <= kRowsOutputMaxBytes;
+}
 
 // K slices of the tensor-core router GEMM (partial sums, combined when picking candidates)
 inline int router_kslices(int d) { return d / 64 >= 16 ? 4 : (d / 64 >= 4 ? 2 : 1); }
@@ -589,6 +591,7 @@ struct FfnArgs {
     uint8_t* ws;
     WsLayout L;
     int num_sms;
+    bool rows_out;             // down projection: weighted rows (true) or reduce-adds into the sum
 };
 
 cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);

@@ -107,3 +107,12 @@ def test_static_scratch_rejects_what_does_not_fit(lib):
     two = _lib.moe_shape(2, 1024, 256, 8, 256, 256, 64)
     rc = lib.moe_forward_decode_static(ctypes.byref(two), fake, fake, None, fake, fake, ctypes.byref(rt), fake, None)
     assert rc == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_deterministic_option_is_validated(lib):
+    """moe_options.deterministic takes 0 or 1; anything else is an argument error (no GPU)."""
+    s = _lib.moe_shape(4096, 2048, 256, 8, 512, 512, 64)
+    for v, ok in ((0, True), (1, True), (2, False), (-1, False)):
+        o = _lib.moe_options(32, 1, 0, v)
+        n = lib.moe_workspace_bytes(ctypes.byref(s), ctypes.byref(o))
+        assert (n > 0) == ok, (v, n)

@@ -237,3 +237,25 @@ def test_default_scales_use_the_denormal_encoding():
     shp = moe.shape(8, sh.d, sh.E, sh.k, sh.I, sh.I_shared)
     dl = DeviceLayer(shp, configs.make_layer(wl))
     assert int(dl.packed_routed[:4].view(torch.int32).item()) == 0
+
+
+def test_output_paths_and_deterministic_mode():
+    """A 1024-token chunk: its weighted rows (9 x 1024 x 2048 fp32 = 75 MB) exceed what the
+    default keeps in L2, so the down projection adds into the fp32 sum; deterministic = 1 takes
+    the rows path with the fixed-order combine.  Both match the oracle (sampled tokens), and the
+    deterministic mode gives identical bits on a repeated call."""
+    wl = configs.custom_workload("t1024_d2048_i512", T=1024, d=2048, I=512, seed=11)
+    shp, lay, x, dl = _setup(wl)
+    xd = to_dev(x)
+    ref = oracle.route(x, lay.w_router, lay.logit_bias)
+    toks = np.unique(np.concatenate([[0, shp.T - 1], np.random.default_rng(3).choice(shp.T, 14, replace=False)]))
+    toks = toks.astype(np.int32)
+    out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared, toks)
+    ys = {}
+    for det in (0, 1, 1):
+        opts = moe.options(deterministic=det)
+        rt, ws, y = run_forward(shp, dl, xd, opts=opts)
+        assert_routing_equal(routing_to_host(rt, shp.T), ref)
+        assert_output_close(y_to_f64(y)[toks], out_ref, f"deterministic={det}")
+        ys.setdefault(det, []).append(y.clone())
+    assert torch.equal(ys[1][0], ys[1][1]), "deterministic mode: repeated calls differ"
