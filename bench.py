@@ -7,8 +7,9 @@ synthetic input of the workload.  Default workload: the 512-token prefill chunk 
 256 experts, top-8, I=512 + shared expert), whose 455 MB of 4-bit weights exceed L2, so every
 step streams its inputs from HBM (a workload whose layer fits in L2 rotates through enough
 independent layer copies to exceed it).  Timing: W untimed steps, then K steps between CUDA events on
-the launching stream (each step is replayed from CUDA graphs of the library calls), barrier +
-synchronize on both sides, max over ranks.  Multi-GPU (torchrun): every rank runs its own
+the launching stream (each step is replayed from a CUDA graph of the library calls; every 8th
+step replays one graph per phase instead, with events between the phases that give the
+gate/up and down kernel times), barrier + synchronize on both sides, max over ranks.  Multi-GPU (torchrun): every rank runs its own
 chunks (weak scaling, no collective on the data path).
 
 --impl reference times the CPU oracle on bounded samples of the same workload on the host
@@ -212,28 +213,41 @@ def run_ours(args, rank, world, local):
                 for f in calls_for(L[gi % layers], xs[gi % len(xs)]).values():
                     f()
             stream.synchronize()
+            # per set: the whole step as one graph (consecutive kernels overlap their prologues
+            # through programmatic dependent launch) and the four phases as separate graphs, which
+            # every PROBE-th timed step runs instead, with events between them for the kernel times
             graphs = []
             for gi in range(nsets):
                 if gi == 0:
                     n0 = moe.moe_launch_count()
                 gc = {}
-                for name, f in calls_for(L[gi % layers], xs[gi % len(xs)]).items():
+                calls = calls_for(L[gi % layers], xs[gi % len(xs)])
+                for name, f in calls.items():
                     g = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g, stream=stream):
                         f()
                     gc[name] = g
-                graphs.append(gc)
                 if gi == 0:
                     launches_one_chunk = moe.moe_launch_count() - n0
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for f in calls.values():
+                        f()
+                gc["step"] = g
+                graphs.append(gc)
     launches_per_step = moe.moe_launch_count() - n0 if decode else launches_one_chunk
     torch.cuda.synchronize()
 
     # prefill: a step runs the graphs of its chunk, which read the chunk where it resides;
     # decode: a step copies its token's activations (4 KB) into the graph's input buffer first
+    PROBE = 8
+
     def step(s, ev=None):
         if decode:
             x_in.copy_(x_all[s % nsteps_x:s % nsteps_x + 1], non_blocking=True)
             graphs["step"].replay()
+        elif ev is None:
+            graphs[s % len(graphs)]["step"].replay()
         else:
             gc = graphs[s % len(graphs)]
             gc["route"].replay()
@@ -266,7 +280,8 @@ def run_ours(args, rank, world, local):
             K = int(min(20000, max(20, 1500.0 / max(per, 1e-3))))
         else:
             K = args.steps
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)] if not decode else None
+        evs = {s: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for s in range(0, K, PROBE)} \
+            if not decode else {}
         clocks = ClockSampler(local)
         clocks.start()
         time.sleep(0.15)
@@ -277,7 +292,7 @@ def run_ours(args, rank, world, local):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for s in range(K):
-            step(s, evs[s] if evs else None)
+            step(s, evs.get(s))
         t1.record(stream)
         t1.synchronize()
         torch.cuda.synchronize()
@@ -313,7 +328,7 @@ def run_ours(args, rank, world, local):
     else:
         value = world * T * K / (ms_total / 1000.0)
         res.update(value=value, unit="routed tokens/s", higher_is_better=True)
-        ph = np.array([[evs[s][0].elapsed_time(evs[s][1]), evs[s][1].elapsed_time(evs[s][2])] for s in range(K)])
+        ph = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in evs.values()])
         gu_ms, dn_ms = float(ph[:, 0].mean()), float(ph[:, 1].mean())
         counts = rt.counts.cpu().numpy()
         A = algorithmic_counts(shp, counts)

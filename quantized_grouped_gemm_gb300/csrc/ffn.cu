@@ -219,8 +219,6 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_bl, TmParams p) {
     using C = TmCfg<kDown>;
     extern __shared__ uint8_t smem_dyn[];
-    const int num = *p.num_tiles;
-    if ((int)blockIdx.x >= num) return;
     uint8_t* smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     uint8_t* xring = smem + C::x_off;
     uint8_t* cring = smem + C::c_off;
@@ -251,6 +249,14 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = b->tmem_slot;
+    // the prologue above may overlap the previous kernel; the tile list comes from it
+    pdl_wait();
+    pdl_launch_dependents();
+    const int num = *p.num_tiles;
+    if ((int)blockIdx.x >= num) {
+        if (warp == kTmMmaWarp) tmem_dealloc(tmem, 512);
+        return;
+    }
 
     if (warp == kTmCodeWarp) {
         // packed codes of every (tile, K block), up to RC K blocks ahead of the dequant
@@ -574,6 +580,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 __global__ void combine_rows_kernel(const float4* __restrict__ Y, const int32_t* __restrict__ pos,
                                     uint2* __restrict__ y, int T, int d4, int k) {
     const size_t n = (size_t)T * d4, tile4 = (size_t)(k + 1) * T * 32;   // float4s of a 128-column tile
+    pdl_wait();
+    pdl_launch_dependents();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / d4), c = (int)(i % d4);
         const float4* Yc = Y + (size_t)(c >> 5) * tile4 + (c & 31);
@@ -635,10 +643,9 @@ cudaError_t launch_gate_up_tm(const FfnArgs& a, cudaStream_t st, unsigned long l
     if (err == cudaSuccess) err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, kTmBox);
     if (err == cudaSuccess) err = make_tmap_bf16_2d(&tm_xl, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, kTmBoxL);
     if (err != cudaSuccess) return err;
-    ffn_tm_kernel<false><<<a.num_sms, kTmThreads, tm_smem_bytes<false>(), st>>>(tm_xs, tm_xsl, tm_x, tm_xl,
-                                                                              make_tm_params(a, true));
     *launches += 1;
-    return cudaGetLastError();
+    return launch_with_pdl(ffn_tm_kernel<false>, dim3(a.num_sms), dim3(kTmThreads), tm_smem_bytes<false>(), st, tm_xs,
+                           tm_xsl, tm_x, tm_xl, make_tm_params(a, true));
 }
 
 cudaError_t launch_down_tm(const FfnArgs& a, cudaStream_t st, unsigned long long* launches) {
@@ -651,10 +658,9 @@ cudaError_t launch_down_tm(const FfnArgs& a, cudaStream_t st, unsigned long long
         err = make_tmap_bf16_2d(&tm_hl, a.ws + a.L.H, (uint64_t)(a.k + 1) * a.T, 2 * (uint64_t)a.I,
                                 (uint64_t)a.I * 4, kBK, kTmBoxL);
     if (err != cudaSuccess) return err;
-    ffn_tm_kernel<true><<<a.num_sms, kTmThreads, tm_smem_bytes<true>(), st>>>(tm_h, tm_hl, tm_h, tm_hl,
-                                                                             make_tm_params(a, false));
     *launches += 1;
-    return cudaGetLastError();
+    return launch_with_pdl(ffn_tm_kernel<true>, dim3(a.num_sms), dim3(kTmThreads), tm_smem_bytes<true>(), st, tm_h,
+                           tm_hl, tm_h, tm_hl, make_tm_params(a, false));
 }
 
 }  // namespace moe
@@ -664,10 +670,9 @@ cudaError_t launch_combine_rows(int T, int d, int k, const float* Y, const int32
                                 unsigned long long* launches) {
     const size_t n = (size_t)T * (d / 4);
     const int blocks = (int)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
-    combine_rows_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(Y), pos, reinterpret_cast<uint2*>(y), T,
-                                                d / 4, k);
     *launches += 1;
-    return cudaGetLastError();
+    return launch_with_pdl(combine_rows_kernel, dim3(blocks), dim3(256), 0, st, reinterpret_cast<const float4*>(Y), pos,
+                           reinterpret_cast<uint2*>(y), T, d / 4, k);
 }
 }  // namespace moe
 
@@ -678,6 +683,8 @@ cudaError_t launch_combine_rows(int T, int d, int k, const float* Y, const int32
 namespace moe {
 namespace {
 __global__ void combine_kernel(float4* __restrict__ acc, uint2* __restrict__ y, size_t n4) {
+    pdl_wait();
+    pdl_launch_dependents();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         const float4 v = acc[i];
         y[i] = make_uint2((uint32_t)f32_to_bf16_rn(v.x) | ((uint32_t)f32_to_bf16_rn(v.y) << 16),
@@ -690,9 +697,8 @@ __global__ void combine_kernel(float4* __restrict__ acc, uint2* __restrict__ y, 
 cudaError_t launch_combine(int T, int d, const float* acc, uint16_t* y, cudaStream_t st, unsigned long long* launches) {
     const size_t n4 = (size_t)T * d / 4;
     const int blocks = (int)((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096);
-    combine_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<float4*>(const_cast<float*>(acc)), reinterpret_cast<uint2*>(y),
-                                           n4);
     *launches += 1;
-    return cudaGetLastError();
+    return launch_with_pdl(combine_kernel, dim3(blocks), dim3(256), 0, st, reinterpret_cast<float4*>(const_cast<float*>(acc)),
+                           reinterpret_cast<uint2*>(y), n4);
 }
 }  // namespace moe

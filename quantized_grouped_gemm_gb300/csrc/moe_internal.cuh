@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -96,8 +98,18 @@ inline bool ffn_rows_output(int T, int d, int k, bool deterministic) {
     return deterministic || (size_t)(k + 1) * T * d * 4 <= kRowsOutputMaxBytes;
 }
 
-// K slices of the tensor-core router GEMM (partial sums, combined when picking candidates)
-inline int router_kslices(int d) { return d / 64 >= 16 ? 4 : (d / 64 >= 4 ? 2 : 1); }
+// K slices of the tensor-core router GEMM (partial sums, combined when picking candidates):
+// enough that (token blocks of 128) x slices reaches ~128 CTAs, at most 16 and at most one
+// slice per 64-column K block
+#ifndef MOE_ROUTER_KS_MAX
+#define MOE_ROUTER_KS_MAX 16
+#endif
+inline int router_kslices(int T, int d) {
+    const int blocks = (T + 127) / 128, kb = d / 64;
+    int ks = 1;
+    while (ks < MOE_ROUTER_KS_MAX && ks < kb && blocks * ks < 128) ks *= 2;
+    return ks;
+}
 
 inline int gemm_ntile_bound(int rows_total, int groups) {
     // tiles of <= kMaxN rows, near-equal split per group: at most rows/kMaxN + groups
@@ -123,7 +135,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
     L.max_dn = (routed_nd + shared_nd) * (d / 256);
     size_t o = 0;
     L.status = o; o = align_up(o + 64 * 4, 256);
-    L.rpart = o; o = align_up(o + (size_t)router_kslices(d) * T * E * 4, 256);
+    L.rpart = o; o = align_up(o + (size_t)router_kslices(T, d) * T * E * 4, 256);
     L.wnorm = o; o = align_up(o + (size_t)E * 4, 256);
     L.blk = o; o = align_up(o + (size_t)2 * L.nblk * E * 4, 256);
     L.gu_tiles = o; o = align_up(o + (size_t)L.max_gu * 16, 256);
@@ -419,11 +431,38 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     return v;
 }
 
+__device__ __forceinline__ float4 ld_nc_f4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void set_status(int* status, int bits) { atomicOr(status, bits); }
 
 // Programmatic dependent launch: wait for the previous grid's results / let the next grid start.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with programmatic stream serialization: the kernel may start (and run its prologue)
+// while the previous kernel on the stream finishes; every such kernel calls pdl_wait() before
+// its first global memory access and pdl_launch_dependents() only after that wait, so at most
+// one launch waits ahead and every kernel still sees all earlier ones complete.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_with_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
 
 // Order-preserving key: larger logit first, then lower expert index.  NaN counts as -inf
 // and -0 as +0 (they compare equal to +0).

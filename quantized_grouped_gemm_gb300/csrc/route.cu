@@ -59,6 +59,8 @@ __device__ __forceinline__ float warp_pinned_logit(const uint16_t* xrow, const u
 // router_wnorm: ||W_r[e]||_2 (fp32) for every expert; one warp per expert.
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) router_wnorm(RouteArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31, e = blockIdx.x * 4 + (threadIdx.x >> 5);
     float s = 0.f;
     for (int c = 8 * lane; c < a.d; c += 256) {
@@ -111,6 +113,8 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    pdl_wait();
+    pdl_launch_dependents();
     if (warp == 0) {
         if (lane == 0) {
             prefetch_tmap(&tm_x);
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------------------------------
 // route_certify_topk (the bound): for each token, with l~[e] the tensor-core logit (sum of the
 // K slices, + bias) and
-//   delta[e] = c * ||x_t|| * ||W_r[e]||,  c = 2 * ((d + 4 + 35) * 2^-23)  (+ a bias term),
+//   delta[e] = c * ||x_t|| * ||W_r[e]||,  c = 2 * ((d + KS + 35) * 2^-23)  (+ a bias term),
 // which bounds |l~[e] - l[e]| for the fixed-order logit l (any fp32 summation of d exact
 // products errs by at most ~d*2^-23 * sum|x w| <= d*2^-23 ||x|| ||w||; the fixed order by
 // 69*2^-24 of the same; factor 2 for margin):
@@ -194,50 +198,72 @@ __global__ void __launch_bounds__(192, 1)
 // are recomputed.  The result equals top-8 over all 256 exact logits.
 // Also writes the block's per-expert counts.
 // ---------------------------------------------------------------------------------------
-// Exact logits (fixed order, as warp_pinned_logit) of two experts for the token row held in
-// registers, with both rows' loads issued before the arithmetic.
-template <int NI>
-__device__ __forceinline__ void warp_pinned_logit2(const uint4 (&xv)[8], const uint16_t* w0, const uint16_t* w1,
-                                                   int lane, float& l0, float& l1) {
-    uint4 a[NI], b[NI];
+// Exact logits (fixed order, as warp_pinned_logit) of G experts for the token row held in
+// registers, with all G rows' loads issued before the arithmetic.
+template <int NI, int G>
+__device__ __forceinline__ void warp_pinned_logits(const uint4 (&xv)[8], const uint16_t* const (&w)[G], int lane,
+                                                   float (&l)[G]) {
+    uint4 a[G][NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+#pragma unroll
+        for (int g = 0; g < G; ++g) a[g][i] = ld_nc_v4(w[g] + 256 * i + 8 * lane);
+    float p[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) p[g] = 0.f;
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-        a[i] = ld_nc_v4(w0 + 256 * i + 8 * lane);
-        b[i] = ld_nc_v4(w1 + 256 * i + 8 * lane);
-    }
-    float p = 0.f, q = 0.f;
 #pragma unroll
-    for (int i = 0; i < NI; ++i) {
-        p = fmaf(bf16lo(xv[i].x), bf16lo(a[i].x), p);  q = fmaf(bf16lo(xv[i].x), bf16lo(b[i].x), q);
-        p = fmaf(bf16hi(xv[i].x), bf16hi(a[i].x), p);  q = fmaf(bf16hi(xv[i].x), bf16hi(b[i].x), q);
-        p = fmaf(bf16lo(xv[i].y), bf16lo(a[i].y), p);  q = fmaf(bf16lo(xv[i].y), bf16lo(b[i].y), q);
-        p = fmaf(bf16hi(xv[i].y), bf16hi(a[i].y), p);  q = fmaf(bf16hi(xv[i].y), bf16hi(b[i].y), q);
-        p = fmaf(bf16lo(xv[i].z), bf16lo(a[i].z), p);  q = fmaf(bf16lo(xv[i].z), bf16lo(b[i].z), q);
-        p = fmaf(bf16hi(xv[i].z), bf16hi(a[i].z), p);  q = fmaf(bf16hi(xv[i].z), bf16hi(b[i].z), q);
-        p = fmaf(bf16lo(xv[i].w), bf16lo(a[i].w), p);  q = fmaf(bf16lo(xv[i].w), bf16lo(b[i].w), q);
-        p = fmaf(bf16hi(xv[i].w), bf16hi(a[i].w), p);  q = fmaf(bf16hi(xv[i].w), bf16hi(b[i].w), q);
+        for (int g = 0; g < G; ++g) {
+            p[g] = fmaf(bf16lo(xv[i].x), bf16lo(a[g][i].x), p[g]);
+            p[g] = fmaf(bf16hi(xv[i].x), bf16hi(a[g][i].x), p[g]);
+            p[g] = fmaf(bf16lo(xv[i].y), bf16lo(a[g][i].y), p[g]);
+            p[g] = fmaf(bf16hi(xv[i].y), bf16hi(a[g][i].y), p[g]);
+            p[g] = fmaf(bf16lo(xv[i].z), bf16lo(a[g][i].z), p[g]);
+            p[g] = fmaf(bf16hi(xv[i].z), bf16hi(a[g][i].z), p[g]);
+            p[g] = fmaf(bf16lo(xv[i].w), bf16lo(a[g][i].w), p[g]);
+            p[g] = fmaf(bf16hi(xv[i].w), bf16hi(a[g][i].w), p[g]);
+        }
     }
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) {
-        p = p + __shfl_xor_sync(0xffffffffu, p, m);
-        q = q + __shfl_xor_sync(0xffffffffu, q, m);
+#pragma unroll
+        for (int g = 0; g < G; ++g) p[g] = p[g] + __shfl_xor_sync(0xffffffffu, p[g], m);
     }
-    l0 = p;
-    l1 = q;
+#pragma unroll
+    for (int g = 0; g < G; ++g) l[g] = p[g];
 }
 
-__device__ __forceinline__ void pinned_logit_pair(const uint4 (&xv)[8], const uint16_t* xrow, const uint16_t* w_router,
-                                                  int d, int e0, int e1, int lane, float& l0, float& l1) {
-    const uint16_t* w0 = w_router + (size_t)e0 * d;
-    const uint16_t* w1 = w_router + (size_t)e1 * d;
+template <int G>
+__device__ __forceinline__ void pinned_logit_group(const uint4 (&xv)[8], const uint16_t* xrow, const uint16_t* w_router,
+                                                   int d, const int (&e)[G], int lane, float (&l)[G]) {
+    const uint16_t* w[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) w[g] = w_router + (size_t)e[g] * d;
     switch (d / 256) {
-        case 1: warp_pinned_logit2<1>(xv, w0, w1, lane, l0, l1); return;
-        case 2: warp_pinned_logit2<2>(xv, w0, w1, lane, l0, l1); return;
-        case 4: warp_pinned_logit2<4>(xv, w0, w1, lane, l0, l1); return;
-        case 8: warp_pinned_logit2<8>(xv, w0, w1, lane, l0, l1); return;
+        case 1: warp_pinned_logits<1, G>(xv, w, lane, l); return;
+        case 2: warp_pinned_logits<2, G>(xv, w, lane, l); return;
+        case 4: warp_pinned_logits<4, G>(xv, w, lane, l); return;
+        case 8: warp_pinned_logits<8, G>(xv, w, lane, l); return;
         default:
-            l0 = warp_pinned_logit(xrow, w0, d, lane, nullptr);
-            l1 = warp_pinned_logit(xrow, w1, d, lane, nullptr);
+#pragma unroll
+            for (int g = 0; g < G; ++g) l[g] = warp_pinned_logit(xrow, w[g], d, lane, nullptr);
+    }
+}
+
+// Sum of the KS K-slice partial logits of experts 8*lane .. 8*lane+7 (slice order).
+template <int KS>
+__device__ __forceinline__ void sum_kslices(const float* p, size_t qstride, float (&lt)[8]) {
+    float4 v[KS][2];
+#pragma unroll
+    for (int q = 0; q < KS; ++q) {
+        v[q][0] = ld_nc_f4(p + q * qstride);
+        v[q][1] = ld_nc_f4(p + q * qstride + 4);
+    }
+#pragma unroll
+    for (int q = 0; q < KS; ++q) {
+        lt[0] += v[q][0].x; lt[1] += v[q][0].y; lt[2] += v[q][0].z; lt[3] += v[q][0].w;
+        lt[4] += v[q][1].x; lt[5] += v[q][1].y; lt[6] += v[q][1].z; lt[7] += v[q][1].w;
     }
 }
 
@@ -253,12 +279,14 @@ __device__ __forceinline__ float key32_logit(uint32_t k) {
 }
 
 // ---------------------------------------------------------------------------------------
-// route_certify_topk: one warp per token, kCertTokens tokens per CTA.
-// From the tensor-core partial logits l~ and the bound delta of each expert it keeps the
-// candidates l~ + delta >= lo with lo = (8th largest l~) - max delta (at least eight experts
-// have an exact logit >= lo, so no other expert can be in the exact top-8), recomputes their
-// exact logits in the fixed order, two at a time, and takes the top-k among them.  More than
-// 32 candidates: all 256 are recomputed.  Per-block expert counts are added for the scan.
+// route_certify_topk: one warp per token, kCertTokens tokens per CTA; lane l holds experts
+// 8l .. 8l+7.  From the tensor-core partial logits l~ and the bound delta of each expert it
+// keeps the candidates l~ + delta >= lo with lo = (8th largest l~) - max delta (at least eight
+// experts have an exact logit >= lo, so no other expert can be in the exact top-8),
+// recomputes their exact logits in the fixed order, kCertGroup at a time (each warp's time is
+// a chain of L2 round trips, so every load of a group is in flight at once), and takes the
+// top-k among them.  More than 32 candidates: all 256 are recomputed.  Per-block expert counts
+// are added for the scan.
 // ---------------------------------------------------------------------------------------
 #ifndef MOE_CERT_TOKENS
 #define MOE_CERT_TOKENS 8
@@ -268,6 +296,11 @@ __device__ __forceinline__ float key32_logit(uint32_t k) {
 // other at 512 tokens, 8 the fastest); divides the 32-token routing block
 constexpr int kCertTokens = MOE_CERT_TOKENS;
 static_assert(kRouteBlockTokens % kCertTokens == 0, "certify tokens per CTA");
+#ifndef MOE_CERT_GROUP
+#define MOE_CERT_GROUP 4
+#endif
+constexpr int kCertGroup = MOE_CERT_GROUP;   // exact logits per round
+static_assert(kCertGroup >= 1 && 256 % kCertGroup == 0, "certify group");
 
 __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs a, int KS) {
     __shared__ uint32_t s_mask[256];
@@ -277,7 +310,9 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
     const int tok = blockIdx.x * kCertTokens + warp;
     const float* part = reinterpret_cast<const float*>(a.ws + a.L.rpart);
     const float* wnorm = reinterpret_cast<const float*>(a.ws + a.L.wnorm);
-    const float c = 2.0f * (float)(a.d + 4 + 35) * 1.1920928955078125e-7f;   // 2^-23
+    const float c = 2.0f * (float)(a.d + KS + 35) * 1.1920928955078125e-7f;   // 2^-23
+    pdl_wait();
+    pdl_launch_dependents();
     for (int i = threadIdx.x; i < 256; i += blockDim.x) s_mask[i] = 0;
     __syncthreads();
     if (tok < a.T) {
@@ -290,13 +325,22 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
             xv[i] = make_uint4(0, 0, 0, 0);
             if (i < a.d / 256) xv[i] = ld_nc_v4(xrow + 256 * i + 8 * lane);
         }
-        float lt[8], dl[8];
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const int e = lane + 32 * s;
-            float v = 0.f;
-            for (int q = 0; q < KS; ++q) v += part[((size_t)q * a.T + tok) * 256 + e];
-            lt[s] = v;
+        float lt[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, dl[8], wn[8];
+        {
+            const float* p = part + (size_t)tok * 256 + 8 * lane;
+            const size_t qs = (size_t)a.T * 256;
+            switch (KS) {
+                case 1: sum_kslices<1>(p, qs, lt); break;
+                case 2: sum_kslices<2>(p, qs, lt); break;
+                case 4: sum_kslices<4>(p, qs, lt); break;
+                case 8: sum_kslices<8>(p, qs, lt); break;
+                case 16: sum_kslices<16>(p, qs, lt); break;
+                default:
+                    for (int q = 0; q < KS; ++q) sum_kslices<1>(p + q * qs, qs, lt);
+            }
+            const float4 w0 = ld_nc_f4(wnorm + 8 * lane), w1 = ld_nc_f4(wnorm + 8 * lane + 4);
+            wn[0] = w0.x; wn[1] = w0.y; wn[2] = w0.z; wn[3] = w0.w;
+            wn[4] = w1.x; wn[5] = w1.y; wn[6] = w1.z; wn[7] = w1.w;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -319,10 +363,10 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
         uint32_t key[8];
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-            const int e = lane + 32 * s;
+            const int e = 8 * lane + s;
             const float b = a.bias ? a.bias[e] : 0.f;
             lt[s] += b;
-            dl[s] = c * nx * wnorm[e] + 4.7683716e-7f * (fabsf(lt[s]) + fabsf(b) + 1.0f);   // + 2^-21 (|l|+|b|+1)
+            dl[s] = c * nx * wn[s] + 4.7683716e-7f * (fabsf(lt[s]) + fabsf(b) + 1.0f);   // + 2^-21 (|l|+|b|+1)
             dmax = fmaxf(dmax, dl[s]);
             key[s] = logit_key32(lt[s]);
         }
@@ -337,11 +381,11 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
             int mine = 0x7fffffff;
 #pragma unroll
             for (int s = 7; s >= 0; --s)
-                if (key[s] == top) mine = 32 * s + lane;
+                if (key[s] == top) mine = 8 * lane + s;
             const int who = __reduce_min_sync(0xffffffffu, mine);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                if (32 * s + lane == who) key[s] = 0u;
+                if (8 * lane + s == who) key[s] = 0u;
         }
         const float lo = __fsub_rd(key32_logit(top), dmax);
         uint32_t cm[8];
@@ -355,23 +399,27 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
         int e_out;
         float w_out;
         if (ncand <= 32) {
-            // candidate j (ascending expert) goes to lane j
+            // candidate j goes to lane j (listed by s, then lane)
             int before = 0;
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
-                if (cm[s] >> lane & 1u) s_cand[warp][before + __popc(cm[s] & ((1u << lane) - 1u))] = lane + 32 * s;
+                if (cm[s] >> lane & 1u) s_cand[warp][before + __popc(cm[s] & ((1u << lane) - 1u))] = 8 * lane + s;
                 before += __popc(cm[s]);
             }
             __syncwarp();
             int my_e = -1;
             float my_l = -INFINITY;
-            for (int j0 = 0; j0 < ncand; j0 += 2) {
-                const int e0 = s_cand[warp][j0], e1 = j0 + 1 < ncand ? s_cand[warp][j0 + 1] : e0;
-                float l0, l1;
-                pinned_logit_pair(xv, xrow, a.w_router, a.d, e0, e1, lane, l0, l1);
-                if (a.bias) { l0 = l0 + a.bias[e0]; l1 = l1 + a.bias[e1]; }
-                if (lane == j0) { my_e = e0; my_l = l0; }
-                if (lane == j0 + 1) { my_e = e1; my_l = l1; }
+            for (int j0 = 0; j0 < ncand; j0 += kCertGroup) {
+                int eg[kCertGroup];
+#pragma unroll
+                for (int g = 0; g < kCertGroup; ++g) eg[g] = s_cand[warp][min(j0 + g, ncand - 1)];
+                float lg[kCertGroup];
+                pinned_logit_group<kCertGroup>(xv, xrow, a.w_router, a.d, eg, lane, lg);
+#pragma unroll
+                for (int g = 0; g < kCertGroup; ++g) {
+                    const float v = a.bias ? lg[g] + a.bias[eg[g]] : lg[g];
+                    if (lane == j0 + g && j0 + g < ncand) { my_e = eg[g]; my_l = v; }
+                }
             }
             // top-k among the exact candidate logits, one per lane
             uint32_t k1 = my_e >= 0 ? logit_key32(my_l) : 0u;
@@ -392,12 +440,15 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
             e_out = sel_e;
             w_out = ex / den;
         } else {
-            for (int e = 0; e < 256; e += 2) {
-                float l0, l1;
-                pinned_logit_pair(xv, xrow, a.w_router, a.d, e, e + 1, lane, l0, l1);
-                if (a.bias) { l0 = l0 + a.bias[e]; l1 = l1 + a.bias[e + 1]; }
-                if (lane == (e & 31)) s_all[warp][e] = l0;
-                if (lane == ((e + 1) & 31)) s_all[warp][e + 1] = l1;
+            for (int e0 = 0; e0 < 256; e0 += kCertGroup) {
+                int eg[kCertGroup];
+#pragma unroll
+                for (int g = 0; g < kCertGroup; ++g) eg[g] = e0 + g;
+                float lg[kCertGroup];
+                pinned_logit_group<kCertGroup>(xv, xrow, a.w_router, a.d, eg, lane, lg);
+#pragma unroll
+                for (int g = 0; g < kCertGroup; ++g)
+                    if (lane == ((e0 + g) & 31)) s_all[warp][e0 + g] = a.bias ? lg[g] + a.bias[e0 + g] : lg[g];
             }
             __syncwarp();
             warp_topk256(s_all[warp], a.k, lane, e_out, w_out);
@@ -444,6 +495,8 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     __shared__ int s_tot[4];   // [0] block-map tiles, [1] gate/up blocks, [2] down blocks
     __shared__ int s_part[4][256];
     __shared__ int s_off[256];
+    pdl_wait();
+    pdl_launch_dependents();
     const int E = 256;
     const int e = threadIdx.x & 255, part = threadIdx.x >> 8;
     int32_t* blk_counts = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
@@ -573,6 +626,8 @@ __global__ void __launch_bounds__(256) route_scatter(RouteArgs a) {
     const int ntok = min(kRouteBlockTokens, a.T - t0);
     const int32_t* blk_base = reinterpret_cast<const int32_t*>(a.ws + a.L.blk) + (size_t)a.L.nblk * E;
     int* status = reinterpret_cast<int*>(a.ws + a.L.status);
+    pdl_wait();
+    pdl_launch_dependents();
     s_mask[threadIdx.x] = 0;
     __syncthreads();
     const int tl = threadIdx.x / 8, j = threadIdx.x % 8;   // k == 8
@@ -758,19 +813,22 @@ cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned l
         attr = true;
     }
     const int nblk = a.L.nblk;
-    const int KS = router_kslices(a.d);
+    const int KS = router_kslices(a.T, a.d);
     CUtensorMap tm_x, tm_w;
     cudaError_t err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, 128);
     if (err != cudaSuccess) return err;
     err = make_tmap_bf16_2d(&tm_w, a.w_router, 256, a.d, (uint64_t)a.d * 2, kBK, 256);
     if (err != cudaSuccess) return err;
-    router_wnorm<<<256 / 4, 128, 0, st>>>(a);
-    router_tc<<<dim3((a.T + 127) / 128, KS), 192, kRtSmem, st>>>(tm_x, tm_w, a, KS);
-    route_certify_topk<<<(a.T + kCertTokens - 1) / kCertTokens, 32 * kCertTokens, 0, st>>>(a, KS);
-    route_scan<<<1, 1024, 0, st>>>(a);
-    route_scatter<<<dim3(nblk, a.k), 256, 0, st>>>(a);
     *launches += 5;
-    return cudaGetLastError();
+    if ((err = launch_with_pdl(router_wnorm, dim3(256 / 4), dim3(128), 0, st, a)) != cudaSuccess) return err;
+    if ((err = launch_with_pdl(router_tc, dim3((a.T + 127) / 128, KS), dim3(192), kRtSmem, st, tm_x, tm_w, a, KS)) !=
+        cudaSuccess)
+        return err;
+    if ((err = launch_with_pdl(route_certify_topk, dim3((a.T + kCertTokens - 1) / kCertTokens), dim3(32 * kCertTokens),
+                               0, st, a, KS)) != cudaSuccess)
+        return err;
+    if ((err = launch_with_pdl(route_scan, dim3(1), dim3(1024), 0, st, a)) != cudaSuccess) return err;
+    return launch_with_pdl(route_scatter, dim3(nblk, a.k), dim3(256), 0, st, a);
 }
 
 cudaError_t launch_route_decode(const RouteArgs& a, cudaStream_t st, unsigned long long* launches) {
