@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ablations", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=32)
     return ap.parse_args()
 
@@ -412,6 +413,8 @@ def run_ours(args, rank, world, local):
         res["e2e"] = dict(value=world * T * Ke / (e_ms / 1000.0), unit="routed tokens/s",
                           h2d_bytes_per_step=T * sh.d * 2, d2h_bytes_per_step=T * sh.d * 2,
                           copies="pinned host buffers; copy stream overlapped with compute, two buffers")
+        if not args.no_ablations:
+            res["ablations"] = ablations(moe, shp, L, layers, xs, rt, ws, y, stream, T, world)
     else:
         xh = configs.make_decode_x(wl, 16)
         xh_t = torch.from_numpy(xh.view(np.int16)).pin_memory()
@@ -435,6 +438,49 @@ def run_ours(args, rank, world, local):
         res["e2e"] = dict(value=e_ms * 1000.0 / Ke / layers, unit="us/token/layer",
                           h2d_bytes_per_step=sh.d * 2, d2h_bytes_per_step=sh.d * 2)
     return res, wl
+
+
+def ablations(moe, shp, L, layers, xs, rt, ws, y, stream, T, world, n=100):
+    """Outside the timed region: the step launched eagerly through moe_forward with the default
+    design and with each ablation of it: the host round trip of the routing counts
+    (moe_options.host_routing, one stream synchronisation per step) and dequantisation as a
+    separate pass that writes bf16 weights before the GEMMs (moe_options.unfused_dequant)."""
+    import torch
+
+    def eager(opts, w):
+        def one(s):
+            lw = L[s % layers]
+            moe.moe_forward(shp, xs[s % len(xs)], lw["wr"], lw["bias"], lw["pr"], lw["ps"], rt, w, y, opts, stream)
+        with torch.cuda.stream(stream):
+            for s in range(3):
+                one(s)
+            stream.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for s in range(n):
+                one(s)
+            b.record(stream)
+            b.synchronize()
+        rc, bits = moe.moe_read_status(w, stream)
+        assert rc == moe.MOE_OK, f"device status {rc} bits {bits}"
+        return a.elapsed_time(b) / n
+
+    dev_ms = eager(moe.options(), ws)
+    host_ms = eager(moe.options(host_routing=1), ws)
+    uf = moe.options(unfused_dequant=1)
+    ws_u = moe.workspace(shp, uf)
+    uf_ms = eager(uf, ws_u)
+    del ws_u
+    tok_s = lambda ms: world * T / (ms / 1000.0)
+    return dict(
+        launch=f"eager moe_forward, {n} steps each (no CUDA graph)",
+        default=dict(ms_per_step=dev_ms, value=tok_s(dev_ms)),
+        host_routing=dict(what="counts to the host, scan and block map there, results back, then scatter "
+                               "(one stream sync per step)",
+                          ms_per_step=host_ms, value=tok_s(host_ms), slowdown=host_ms / dev_ms),
+        unfused_dequant=dict(what="every expert's weights of a projection dequantised to bf16 in HBM by a separate "
+                                  "kernel, then streamed by the same grouped GEMM",
+                             ms_per_step=uf_ms, value=tok_s(uf_ms), slowdown=uf_ms / dev_ms))
 
 
 # ------------------------------------------------------------------------------------- oracle

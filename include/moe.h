@@ -117,7 +117,22 @@ typedef struct moe_options {
                                them into the fp32 sum with bulk reduce-adds otherwise (addition
                                order not fixed); 1: always the fixed order, so repeated calls give
                                identical bits (the rows then pass through HBM at large T) */
-    int reserved[4];
+    int host_routing;       /* 0 (default): the routing scan and block map stay on the GPU.
+                               1: an ablation of that design ("GPU-resident routing" on the
+                               page): moe_route copies the per-block expert counts to the host,
+                               computes counts, offsets, block map and GEMM tile lists there,
+                               copies them back and then scatters.  It synchronises the stream
+                               once per call (so it cannot be captured in a CUDA graph) and gives
+                               results identical to 0.  Ignored by the decode path. */
+    int unfused_dequant;    /* 0 (default): weights are dequantised on chip inside the grouped
+                               GEMMs.  1: an ablation of that design ("Dequantize weights during
+                               matrix multiplication" on the page): each FFN call first writes
+                               every expert's weights of that projection as bf16 into the
+                               workspace (about 6 MB per expert at d=2048, I=512; the workspace
+                               grows accordingly, see moe_workspace_bytes) and the GEMM then
+                               streams those.  Same bf16 weights, same results bit for bit.
+                               Ignored by the decode path. */
+    int reserved[2];
 } moe_options;
 
 /* Human-readable text for a return code. */

@@ -66,6 +66,8 @@ struct Opts {
     int decode_max_tokens = 1;
     int decode_path = MOE_DECODE_AUTO;
     bool deterministic = false;
+    bool host_routing = false;
+    bool unfused_dequant = false;
 };
 
 static int get_opts(const moe_options* o, Opts* out) {
@@ -79,6 +81,10 @@ static int get_opts(const moe_options* o, Opts* out) {
         r.decode_path = o->decode_path;
         if (o->deterministic != 0 && o->deterministic != 1) return MOE_ERR_INVALID_ARG;
         r.deterministic = o->deterministic == 1;
+        if (o->host_routing != 0 && o->host_routing != 1) return MOE_ERR_INVALID_ARG;
+        r.host_routing = o->host_routing == 1;
+        if (o->unfused_dequant != 0 && o->unfused_dequant != 1) return MOE_ERR_INVALID_ARG;
+        r.unfused_dequant = o->unfused_dequant == 1;
     }
     *out = r;
     return MOE_OK;
@@ -91,9 +97,14 @@ static int check_routing(const moe_routing* rt) {
     return MOE_OK;
 }
 
-static int check_ws(const moe_shape* s, void* ws, size_t bytes) {
+static size_t ws_bytes_for(const moe_shape& s, const Opts& o) {
+    const WsLayout L = ws_layout(s);
+    return o.unfused_dequant && !(s.T >= 1 && s.T <= o.decode_max_tokens) ? L.total_unfused : L.total;
+}
+
+static int check_ws(const moe_shape* s, void* ws, size_t bytes, const Opts& o) {
     if (!ws || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
-    if (bytes < ws_layout(*s).total) return MOE_ERR_WORKSPACE;
+    if (bytes < ws_bytes_for(*s, o)) return MOE_ERR_WORKSPACE;
     return MOE_OK;
 }
 
@@ -163,7 +174,7 @@ int moe_check_shape(const moe_shape* s) {
 size_t moe_workspace_bytes(const moe_shape* s, const moe_options* o) {
     Opts op;
     if (moe_check_shape(s) != MOE_OK || get_opts(o, &op) != MOE_OK) return 0;
-    return ws_layout(*s).total;
+    return ws_bytes_for(*s, op);
 }
 
 size_t moe_max_tiles(int T, int k, int E, int tile_rows) {
@@ -220,7 +231,7 @@ static int route_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_r
     if ((rc = get_opts(o, &op)) != MOE_OK) return rc;
     if (s->T == 0) return MOE_OK;
     if ((rc = check_routing(rt)) != MOE_OK) return rc;
-    if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
+    if ((rc = check_ws(s, ws, ws_bytes, op)) != MOE_OK) return rc;
     if (!x || !w_router || !aligned(x, 16) || !aligned(w_router, 16) || (bias && !aligned(bias, 4)))
         return MOE_ERR_INVALID_ARG;
     RouteArgs a = route_args(s, x, w_router, bias, rt, ws, op);
@@ -229,8 +240,10 @@ static int route_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_r
         a.pf_bytes = moe_packed_bytes(s, 1, s->I_shared);
     }
     unsigned long long n = 0;
-    cudaError_t e = is_decode(s, op) ? launch_route_decode(a, static_cast<cudaStream_t>(stream), &n)
-                                     : launch_route_prefill(a, static_cast<cudaStream_t>(stream), &n);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = is_decode(s, op)     ? launch_route_decode(a, st, &n)
+                    : op.host_routing ? launch_route_prefill_host(a, st, &n)
+                                      : launch_route_prefill(a, st, &n);
     g_launches += n;
     return cuda_status(e);
 }
@@ -247,7 +260,7 @@ static int ffn_common(const moe_shape* s, const uint16_t* x, const moe_routing* 
     if ((rc = get_opts(o, op)) != MOE_OK) return rc;
     if (s->T == 0) return 1;
     if ((rc = check_routing(rt)) != MOE_OK) return rc;
-    if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
+    if ((rc = check_ws(s, ws, ws_bytes, *op)) != MOE_OK) return rc;
     if (!wr || !wsh || !aligned(wr, 256) || !aligned(wsh, 256)) return MOE_ERR_INVALID_ARG;
     if (need_x && (!x || !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
     if (num_sms() <= 0) return MOE_ERR_CUDA;
@@ -260,6 +273,7 @@ int moe_ffn_gate_up(const moe_shape* s, const uint16_t* x, const moe_routing* rt
     int rc = ffn_common(s, x, rt, wr, wsh, ws, ws_bytes, o, &op, true);
     if (rc != MOE_OK) return rc == 1 ? MOE_OK : rc;
     FfnArgs a = ffn_args(s, x, rt, wr, wsh, ws);
+    a.unfused = op.unfused_dequant;
     unsigned long long n = 0;
     cudaError_t e;
     if (is_decode(s, op)) {
@@ -278,6 +292,7 @@ int moe_ffn_down(const moe_shape* s, const moe_routing* rt, const void* wr, cons
     if (rc != MOE_OK) return rc == 1 ? MOE_OK : rc;
     FfnArgs a = ffn_args(s, nullptr, rt, wr, wsh, ws);
     a.rows_out = ffn_rows_output(s->T, s->d, s->k, op.deterministic);
+    a.unfused = op.unfused_dequant;
     unsigned long long n = 0;
     cudaError_t e;
     if (is_decode(s, op)) {
@@ -303,7 +318,7 @@ int moe_combine(const moe_shape* s, const moe_routing* rt, void* ws, size_t ws_b
     Opts op;
     if ((rc = get_opts(o, &op)) != MOE_OK) return rc;
     if (s->T == 0) return MOE_OK;
-    if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
+    if ((rc = check_ws(s, ws, ws_bytes, op)) != MOE_OK) return rc;
     if (!y || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(*s);
     uint8_t* w8 = static_cast<uint8_t*>(ws);
@@ -332,7 +347,7 @@ int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
         // one launch for the whole token when the shape and the GPU allow it
         if ((rc = moe_check_shape(s)) != MOE_OK) return rc;
         if ((rc = check_routing(rt)) != MOE_OK) return rc;
-        if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
+        if ((rc = check_ws(s, ws, ws_bytes, op)) != MOE_OK) return rc;
         if (!x || !w_router || !wr || !wsh || !y || !aligned(x, 16) || !aligned(w_router, 16) ||
             (bias && !aligned(bias, 4)) || !aligned(wr, 256) || !aligned(wsh, 256) || !aligned(y, 16))
             return MOE_ERR_INVALID_ARG;

@@ -77,7 +77,12 @@ constexpr int kTmBoxL = 64;                   // token rows per large TMA box
 constexpr int kTmKD = 8;                      // "K block done" barriers
 constexpr int kTmXBytes = kMaxN * 128;        // token rows of one K block: 128 rows x 64 bf16
 
-template <bool kDown>
+// Ring chunk of the bf16-weight ablation (moe_options.unfused_dequant): the two 128-row
+// matrices of a K block as dequantised bf16, [matrix][16-byte word w4][row][16 bytes], so the
+// thread of row r reads its 64 weights conflict-free.
+constexpr int kBf16PairBytes = 2 * kTileRows * kBK * 2;
+
+template <bool kDown, bool kBf16 = false>
 struct TmCfg {
     // TMEM: A ring of A slots x 64 columns from column 0, then NDS accumulator slots of 128
     // columns from column DCOL0
@@ -85,15 +90,21 @@ struct TmCfg {
     static constexpr int NDS = kDown ? 3 : 2;
     static constexpr uint32_t DCOL0 = 64u * A;
     static_assert(DCOL0 + 128u * NDS == 512u, "TMEM columns");
-    static constexpr int RX = kDown ? 4 : 8;                 // token-row ring slots
-    static constexpr int RC = kDown ? 6 : 8;                 // packed-code ring slots
+    static constexpr int RX = kDown ? (kBf16 ? 2 : 4) : 8;   // token-row ring slots
+    static constexpr int CH = kBf16 ? kBf16PairBytes : kChunkPairBytes;   // bytes of a weight chunk
+    static constexpr int RC = kBf16 ? (kDown ? 4 : 2) : (kDown ? 6 : 8);  // weight-chunk ring slots
+    // The two dequant sets take alternate K blocks, so with an even ring every slot belongs to
+    // one set, whose parity waits on it are then never more than one phase ahead.  With an odd
+    // ring a set can reach a slot's next parity wait while the other set's block is still
+    // pending there; the wait then passes at once and the ring's barriers fall out of step.
+    static_assert(RC % 2 == 0, "weight-chunk ring slots must come in pairs, one per dequant set");
     static constexpr int PARTS = kDown ? 2 : 1;              // hi, lo halves of h
     static constexpr int XS = PARTS * kTmXBytes;             // bytes of a token-row slot
     // staging of 32 tokens: gate/up bf16 [32][hi 128 | lo 128]; down two buffers of fp32 [32][128]
     static constexpr int STAGE = kDown ? 2 * 32 * 512 : 32 * 512;
     static constexpr int x_off = 0;
     static constexpr int c_off = x_off + RX * XS;
-    static constexpr int stage_off = c_off + RC * kChunkPairBytes;
+    static constexpr int stage_off = c_off + RC * CH;
     static constexpr int tab_off = stage_off + STAGE;        // down: float weight[128], int token[128]
     static constexpr int bar_off = tab_off + 1024;
 };
@@ -105,12 +116,14 @@ struct TmBars {
     int abort;
 };
 
-template <bool kDown>
+template <bool kDown, bool kBf16 = false>
 constexpr int tm_smem_bytes() {
-    return TmCfg<kDown>::bar_off + (int)sizeof(TmBars) + 1024;   // + alignment slack
+    return TmCfg<kDown, kBf16>::bar_off + (int)sizeof(TmBars) + 1024;   // + alignment slack
 }
 static_assert(tm_smem_bytes<false>() <= 232448, "gate/up smem");
 static_assert(tm_smem_bytes<true>() <= 232448, "down smem");
+static_assert(tm_smem_bytes<false, true>() <= 232448, "gate/up smem (bf16 weights)");
+static_assert(tm_smem_bytes<true, true>() <= 232448, "down smem (bf16 weights)");
 
 struct TmParams {
     const uint8_t* w_routed;   // packed stack: [E][tiles][K/64][2][4608]
@@ -213,11 +226,11 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-template <bool kDown>
+template <bool kDown, bool kBf16>
 __global__ void __launch_bounds__(kTmThreads, 1)
     ffn_tm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_al,
                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_bl, TmParams p) {
-    using C = TmCfg<kDown>;
+    using C = TmCfg<kDown, kBf16>;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     uint8_t* xring = smem + C::x_off;
@@ -265,13 +278,13 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             bool ok = true;
             for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
                 const int4 t = p.tiles[tile];
-                const uint8_t* w = t.x < p.E ? p.w_routed + (size_t)(t.x * WT + t.w) * KB * kChunkPairBytes
-                                             : p.w_shared + (size_t)t.w * KB * kChunkPairBytes;
+                const uint8_t* w = t.x < p.E ? p.w_routed + (size_t)(t.x * WT + t.w) * KB * C::CH
+                                             : p.w_shared + (size_t)t.w * KB * C::CH;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int cs = it % C::RC;
                     if (!mbar_wait(&b->c_empty[cs], ((it / C::RC) & 1) ^ 1, abort)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&b->c_full[cs], kChunkPairBytes);
-                    bulk_g2s(cring + cs * kChunkPairBytes, w + (size_t)kb * kChunkPairBytes, kChunkPairBytes,
+                    mbar_arrive_expect_tx(&b->c_full[cs], C::CH);
+                    bulk_g2s(cring + cs * C::CH, w + (size_t)kb * C::CH, C::CH,
                              &b->c_full[cs]);
                     TM_TRACE(TT_PC, it);
                 }
@@ -401,20 +414,35 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                                  (it < (uint32_t)C::A || mbar_wait(&b->kb_done[g % kTmKD], (g / kTmKD) & 1, abort));
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 if (threadIdx.x == 0) TM_TRACE(TT_DW, it);
-                const uint8_t* ch = cring + cs * kChunkPairBytes;
-                const uint4 c0 = *reinterpret_cast<const uint4*>(ch + code_off);
-                const uint4 c1 = *reinterpret_cast<const uint4*>(ch + code_off + 2048);
-                const uint32_t s2 = *reinterpret_cast<const uint16_t*>(ch + sb_off) * 0x10001u;
-                const uint32_t b2 = *reinterpret_cast<const uint16_t*>(ch + sb_off + 256) * 0x10001u;
+                const uint8_t* ch = cring + cs * C::CH;
                 uint32_t v[32];
-                if (denorm) dequant_row64<true>(c0, c1, s2, b2, v);
-                else dequant_row64<false>(c0, c1, s2, b2, v);
+                if constexpr (kBf16) {   // already dequantised: this row's 64 bf16 weights
+                    const uint4* src = reinterpret_cast<const uint4*>(ch + m * (kBf16PairBytes / 2)) + r;
+#pragma unroll
+                    for (int w4 = 0; w4 < 8; ++w4) {
+                        const uint4 q4 = src[w4 * kTileRows];
+                        v[4 * w4] = q4.x; v[4 * w4 + 1] = q4.y; v[4 * w4 + 2] = q4.z; v[4 * w4 + 3] = q4.w;
+                    }
+                } else {
+                    const uint4 c0 = *reinterpret_cast<const uint4*>(ch + code_off);
+                    const uint4 c1 = *reinterpret_cast<const uint4*>(ch + code_off + 2048);
+                    const uint32_t s2 = *reinterpret_cast<const uint16_t*>(ch + sb_off) * 0x10001u;
+                    const uint32_t b2 = *reinterpret_cast<const uint16_t*>(ch + sb_off + 256) * 0x10001u;
+                    if (denorm) dequant_row64<true>(c0, c1, s2, b2, v);
+                    else dequant_row64<false>(c0, c1, s2, b2, v);
+                }
                 __syncwarp();
                 if (threadIdx.x == 0) TM_TRACE(TT_DD, it);
-                if (lane == 0) mbar_arrive(&b->c_empty[cs]);
+                // the dequantisation above consumed the words read from the slot; the bf16 path
+                // only moves them, so it frees the slot once the store has read the registers
+                if (!kBf16 && lane == 0) mbar_arrive(&b->c_empty[cs]);
                 tc_fence_after();   // the MMAs that read this A slot before have completed
                 tmem_st32(trow + 64u * as, v);
                 tmem_st_wait();
+                if constexpr (kBf16) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&b->c_empty[cs]);
+                }
                 if (threadIdx.x == 0) TM_TRACE(TT_DS, it);
                 tc_fence_before();
                 __syncwarp();
@@ -621,20 +649,77 @@ TmParams make_tm_params(const FfnArgs& a, bool gate_up) {
     return p;
 }
 
-template <bool kDown>
+template <bool kDown, bool kBf16>
 cudaError_t set_tm_smem_attr() {
     static bool done = false;
     if (done) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(ffn_tm_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           tm_smem_bytes<kDown>());
+    cudaError_t err = cudaFuncSetAttribute(ffn_tm_kernel<kDown, kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           tm_smem_bytes<kDown, kBf16>());
     if (err == cudaSuccess) done = true;
+    return err;
+}
+
+// bf16-weight ablation ("dequantise, then multiply" as separate passes): every chunk pair of
+// a packed section dequantised to bf16 in the ring-chunk layout of the bf16 kernels, with the
+// fused kernels' exact dequantisation (so the same bf16 weights); one thread per (pair,
+// matrix, row), 16-byte stores that are contiguous across rows.
+__global__ void __launch_bounds__(256) dequant_pairs_kernel(const uint8_t* __restrict__ src, size_t npairs,
+                                                            const int* __restrict__ mode, uint8_t* __restrict__ dst) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const bool denorm = *mode == kScaleDenorm;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < npairs * 256; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t pair = i >> 8;
+        const int m = (int)(i >> 7) & 1, r = (int)i & 127;
+        const uint8_t* ch = src + pair * kChunkPairBytes + m * kChunkBytes;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(ch + r * 16);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(ch + r * 16 + 2048);
+        const uint32_t s2 = *reinterpret_cast<const uint16_t*>(ch + kChunkCodes + 2 * r) * 0x10001u;
+        const uint32_t b2 = *reinterpret_cast<const uint16_t*>(ch + kChunkCodes + 256 + 2 * r) * 0x10001u;
+        uint32_t v[32];
+        if (denorm) dequant_row64<true>(c0, c1, s2, b2, v);
+        else dequant_row64<false>(c0, c1, s2, b2, v);
+        uint4* o = reinterpret_cast<uint4*>(dst + pair * kBf16PairBytes + m * (kBf16PairBytes / 2)) + r;
+#pragma unroll
+        for (int w4 = 0; w4 < 8; ++w4) o[w4 * kTileRows] = make_uint4(v[4 * w4], v[4 * w4 + 1], v[4 * w4 + 2], v[4 * w4 + 3]);
+    }
+}
+
+cudaError_t launch_dequant_pairs(const uint8_t* packed, size_t first_pair, size_t npairs, uint8_t* dst,
+                                 cudaStream_t st, unsigned long long* launches) {
+    const size_t threads = npairs * 256;
+    const int blocks = (int)((threads + 255) / 256 < 8192 ? (threads + 255) / 256 : 8192);
+    *launches += 1;
+    return launch_with_pdl(dequant_pairs_kernel, dim3(blocks), dim3(256), 0, st,
+                           packed + kPackHeader + first_pair * kChunkPairBytes, npairs,
+                           reinterpret_cast<const int*>(packed), dst);
+}
+
+// chunk pairs per expert of a packed buffer: gate/up section, then down section
+size_t gu_pairs(const FfnArgs& a) { return (size_t)(a.I / kTileRows) * (a.d / kBK); }
+size_t dn_pairs(const FfnArgs& a) { return (size_t)(a.d / 256) * (a.I / kBK); }
+
+// bf16-weight ablation: dequantise one section (gate/up or down) of the routed and the shared
+// buffer into the workspace, then point the kernel's weight bases there
+cudaError_t unfused_prepare(const FfnArgs& a, bool gate_up, TmParams& p, cudaStream_t st,
+                            unsigned long long* launches) {
+    const size_t gu = gu_pairs(a), dn = dn_pairs(a), all = gu + dn;
+    uint8_t* wbf = a.ws + a.L.wbf;
+    uint8_t* routed = wbf + (gate_up ? 0 : (size_t)a.E * gu * kBf16PairBytes);
+    uint8_t* shared = wbf + ((size_t)a.E * all + (gate_up ? 0 : gu)) * kBf16PairBytes;
+    cudaError_t err = launch_dequant_pairs(a.w_routed, gate_up ? 0 : (size_t)a.E * gu, (size_t)a.E * (gate_up ? gu : dn),
+                                           routed, st, launches);
+    if (err == cudaSuccess)
+        err = launch_dequant_pairs(a.w_shared, gate_up ? 0 : gu, gate_up ? gu : dn, shared, st, launches);
+    p.w_routed = routed;
+    p.w_shared = shared;
     return err;
 }
 
 }  // namespace
 
 cudaError_t launch_gate_up_tm(const FfnArgs& a, cudaStream_t st, unsigned long long* launches) {
-    cudaError_t err = set_tm_smem_attr<false>();
+    cudaError_t err = a.unfused ? set_tm_smem_attr<false, true>() : set_tm_smem_attr<false, false>();
     if (err != cudaSuccess) return err;
     CUtensorMap tm_xs, tm_xsl, tm_x, tm_xl;
     err = make_tmap_bf16_2d(&tm_xs, a.ws + a.L.xs, (uint64_t)a.k * a.T, a.d, (uint64_t)a.d * 2, kBK, kTmBox);
@@ -643,13 +728,20 @@ cudaError_t launch_gate_up_tm(const FfnArgs& a, cudaStream_t st, unsigned long l
     if (err == cudaSuccess) err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, kTmBox);
     if (err == cudaSuccess) err = make_tmap_bf16_2d(&tm_xl, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, kTmBoxL);
     if (err != cudaSuccess) return err;
+    TmParams p = make_tm_params(a, true);
+    if (a.unfused) {
+        if ((err = unfused_prepare(a, true, p, st, launches)) != cudaSuccess) return err;
+        *launches += 1;
+        return launch_with_pdl(ffn_tm_kernel<false, true>, dim3(a.num_sms), dim3(kTmThreads),
+                               tm_smem_bytes<false, true>(), st, tm_xs, tm_xsl, tm_x, tm_xl, p);
+    }
     *launches += 1;
-    return launch_with_pdl(ffn_tm_kernel<false>, dim3(a.num_sms), dim3(kTmThreads), tm_smem_bytes<false>(), st, tm_xs,
-                           tm_xsl, tm_x, tm_xl, make_tm_params(a, true));
+    return launch_with_pdl(ffn_tm_kernel<false, false>, dim3(a.num_sms), dim3(kTmThreads), tm_smem_bytes<false>(), st,
+                           tm_xs, tm_xsl, tm_x, tm_xl, p);
 }
 
 cudaError_t launch_down_tm(const FfnArgs& a, cudaStream_t st, unsigned long long* launches) {
-    cudaError_t err = set_tm_smem_attr<true>();
+    cudaError_t err = a.unfused ? set_tm_smem_attr<true, true>() : set_tm_smem_attr<true, false>();
     if (err != cudaSuccess) return err;
     CUtensorMap tm_h, tm_hl;
     err = make_tmap_bf16_2d(&tm_h, a.ws + a.L.H, (uint64_t)(a.k + 1) * a.T, 2 * (uint64_t)a.I, (uint64_t)a.I * 4,
@@ -658,9 +750,16 @@ cudaError_t launch_down_tm(const FfnArgs& a, cudaStream_t st, unsigned long long
         err = make_tmap_bf16_2d(&tm_hl, a.ws + a.L.H, (uint64_t)(a.k + 1) * a.T, 2 * (uint64_t)a.I,
                                 (uint64_t)a.I * 4, kBK, kTmBoxL);
     if (err != cudaSuccess) return err;
+    TmParams p = make_tm_params(a, false);
+    if (a.unfused) {
+        if ((err = unfused_prepare(a, false, p, st, launches)) != cudaSuccess) return err;
+        *launches += 1;
+        return launch_with_pdl(ffn_tm_kernel<true, true>, dim3(a.num_sms), dim3(kTmThreads), tm_smem_bytes<true, true>(),
+                               st, tm_h, tm_hl, tm_h, tm_hl, p);
+    }
     *launches += 1;
-    return launch_with_pdl(ffn_tm_kernel<true>, dim3(a.num_sms), dim3(kTmThreads), tm_smem_bytes<true>(), st, tm_h,
-                           tm_hl, tm_h, tm_hl, make_tm_params(a, false));
+    return launch_with_pdl(ffn_tm_kernel<true, false>, dim3(a.num_sms), dim3(kTmThreads), tm_smem_bytes<true>(), st,
+                           tm_h, tm_hl, tm_h, tm_hl, p);
 }
 
 }  // namespace moe

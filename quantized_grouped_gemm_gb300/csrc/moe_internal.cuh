@@ -65,7 +65,10 @@ struct WsLayout {
     size_t dec;         // decode scratch: logits fp32 [8][E], g/u fp32 [8][k+1][2][I]
     size_t fzlog;       // u64 [8][E]: tagged logits of the one-launch decode kernel (eight copies)
     size_t trace;       // tuning builds (MOE_TRACE): 64 KB of phase timestamps
-    size_t total;
+    size_t total;       // bytes of the workspace
+    size_t wbf;         // bf16-weight ablation only (beyond total): every chunk pair of the routed
+                        // then the shared packed buffer, dequantised, 32 KB each
+    size_t total_unfused;
     int nblk, max_gu, max_dn;
 };
 
@@ -152,6 +155,10 @@ inline WsLayout ws_layout(const moe_shape& s) {
     L.trace = o; o += 65536;
 #endif
     L.total = o;
+    // pairs per expert: gate/up (I/128 row tiles x d/64 K blocks), down (d/256 x I/64)
+    const size_t pairs = (size_t)(I / 128) * (d / 64) + (size_t)(d / 256) * (I / 64);
+    L.wbf = align_up(o, 1024);
+    L.total_unfused = L.wbf + (size_t)(E + 1) * pairs * (2 * 128 * 64 * 2);
     return L;
 }
 
@@ -631,9 +638,11 @@ struct FfnArgs {
     WsLayout L;
     int num_sms;
     bool rows_out;             // down projection: weighted rows (true) or reduce-adds into the sum
+    bool unfused;              // ablation: dequantise every weight to bf16 in the workspace first
 };
 
 cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_route_prefill_host(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_route_decode(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_combine(int T, int d, const float* acc, uint16_t* y, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_decode_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);

@@ -21,6 +21,9 @@
 //                      pos and the gathered rows xs.
 // Decode (one launch): route_decode -- a warp per expert logit, the last CTA to finish
 // does top-8 and the metadata for the few tokens.
+#include <algorithm>
+#include <vector>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -828,6 +831,135 @@ cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned l
                                0, st, a, KS)) != cudaSuccess)
         return err;
     if ((err = launch_with_pdl(route_scan, dim3(1), dim3(1024), 0, st, a)) != cudaSuccess) return err;
+    return launch_with_pdl(route_scatter, dim3(nblk, a.k), dim3(256), 0, st, a);
+}
+
+// ---------------------------------------------------------------------------------------
+// Host-round-trip routing (the ablation of "GPU-resident routing"): the same kernels up to
+// the per-block counts; then the counts go to the host, the host computes what route_scan
+// computes (counts, offsets, per-block bases, exported block map, GEMM tile lists), copies it
+// back and the scatter runs.  One stream synchronisation per call.  Results are identical to
+// launch_route_prefill's.
+// ---------------------------------------------------------------------------------------
+namespace {
+struct HostScan {
+    std::vector<int32_t> counts, offsets, base, tiles, gu, dn;
+    int32_t num_tiles = 0, gu_num = 0, dn_num = 0;
+};
+
+// nb near-equal blocks of `rows` rows from r0, each repeated for the mt weight tiles (weight
+// tile innermost), written from list entry `first` on
+void host_split(std::vector<int32_t>& list, int mt, int first, int ex, int r0, int rows, int nb) {
+    const int q = rows / nb, rem = rows % nb;
+    for (int i = 0; i < nb; ++i) {
+        const int n = q + (i < rem ? 1 : 0);
+        for (int m = 0; m < mt; ++m) {
+            int32_t* t = &list[4 * ((size_t)(first + i) * mt + m)];
+            t[0] = ex; t[1] = r0; t[2] = n; t[3] = m;
+        }
+        r0 += n;
+    }
+}
+
+HostScan host_scan(const RouteArgs& a, const std::vector<int32_t>& blk) {
+    const int E = 256, nb = a.L.nblk, BM = a.tile_rows;
+    HostScan h;
+    h.counts.assign(E, 0);
+    h.offsets.assign(E + 1, 0);
+    h.base.assign((size_t)nb * E, 0);
+    for (int b = 0; b < nb; ++b)
+        for (int e = 0; e < E; ++e) h.counts[e] += blk[(size_t)b * E + e];
+    for (int e = 0; e < E; ++e) h.offsets[e + 1] = h.offsets[e] + h.counts[e];
+    for (int e = 0; e < E; ++e) {
+        int r = h.offsets[e];
+        for (int b = 0; b < nb; ++b) {
+            h.base[(size_t)b * E + e] = r;
+            r += blk[(size_t)b * E + e];
+        }
+    }
+    for (int e = 0; e < E; ++e)
+        for (int i = 0; i * BM < h.counts[e]; ++i) {
+            h.tiles.push_back(e);
+            h.tiles.push_back(h.offsets[e] + i * BM);
+            h.tiles.push_back(std::min(BM, h.counts[e] - i * BM));
+        }
+    h.num_tiles = (int32_t)(h.tiles.size() / 3);
+    const int MTgu = a.I / kTileRows, MTdn = a.d / 256;
+    const int nsh = (a.T + kGuRows - 1) / kGuRows, nshd = (a.T + kDnRows - 1) / kDnRows;
+    int ngu = nsh, ndn = nshd;
+    for (int e = 0; e < E; ++e) {
+        ngu += (h.counts[e] + kGuRows - 1) / kGuRows;
+        ndn += (h.counts[e] + kDnRows - 1) / kDnRows;
+    }
+    h.gu.assign(4 * (size_t)ngu * MTgu, 0);
+    h.dn.assign(4 * (size_t)ndn * MTdn, 0);
+    for (int i = 0; i < nsh; ++i) {
+        const int q = a.T / nsh, rem = a.T % nsh;
+        host_split(h.gu, MTgu, i, E, i * q + std::min(i, rem), q + (i < rem ? 1 : 0), 1);
+    }
+    for (int i = 0; i < nshd; ++i) {
+        const int q = a.T / nshd, rem = a.T % nshd;
+        host_split(h.dn, MTdn, i, E, i * q + std::min(i, rem), q + (i < rem ? 1 : 0), 1);
+    }
+    int gb = nsh, db = nshd;
+    for (int e = 0; e < E; ++e) {
+        const int run = h.counts[e], nn = (run + kGuRows - 1) / kGuRows, nd = (run + kDnRows - 1) / kDnRows;
+        if (nn > 0) host_split(h.gu, MTgu, gb, e, h.offsets[e], run, nn);
+        if (nd > 0) host_split(h.dn, MTdn, db, e, h.offsets[e], run, nd);
+        gb += nn;
+        db += nd;
+    }
+    h.gu_num = ngu * MTgu;
+    h.dn_num = ndn * MTdn;
+    return h;
+}
+}  // namespace
+
+cudaError_t launch_route_prefill_host(const RouteArgs& a, cudaStream_t st, unsigned long long* launches) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t err = cudaFuncSetAttribute(router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+        if (err != cudaSuccess) return err;
+        attr = true;
+    }
+    const int nblk = a.L.nblk, E = 256;
+    const int KS = router_kslices(a.T, a.d);
+    CUtensorMap tm_x, tm_w;
+    cudaError_t err = make_tmap_bf16_2d(&tm_x, a.x, a.T, a.d, (uint64_t)a.d * 2, kBK, 128);
+    if (err != cudaSuccess) return err;
+    err = make_tmap_bf16_2d(&tm_w, a.w_router, 256, a.d, (uint64_t)a.d * 2, kBK, 256);
+    if (err != cudaSuccess) return err;
+    *launches += 4;
+    if ((err = launch_with_pdl(router_wnorm, dim3(256 / 4), dim3(128), 0, st, a)) != cudaSuccess) return err;
+    if ((err = launch_with_pdl(router_tc, dim3((a.T + 127) / 128, KS), dim3(192), kRtSmem, st, tm_x, tm_w, a, KS)) !=
+        cudaSuccess)
+        return err;
+    if ((err = launch_with_pdl(route_certify_topk, dim3((a.T + kCertTokens - 1) / kCertTokens), dim3(32 * kCertTokens),
+                               0, st, a, KS)) != cudaSuccess)
+        return err;
+    // the round trip: per-block counts to the host, scan and block map there, results back
+    int32_t* blk_dev = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
+    std::vector<int32_t> blk((size_t)nblk * E);
+    if ((err = cudaMemcpyAsync(blk.data(), blk_dev, blk.size() * 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+        (err = cudaStreamSynchronize(st)) != cudaSuccess)
+        return err;
+    const HostScan h = host_scan(a, blk);
+    auto h2d = [&](void* dst, const void* src, size_t bytes) {
+        return bytes ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st) : cudaSuccess;
+    };
+    if ((err = cudaMemsetAsync(blk_dev, 0, blk.size() * 4, st)) != cudaSuccess ||   // the next call adds into zeros
+        (err = h2d(blk_dev + (size_t)nblk * E, h.base.data(), h.base.size() * 4)) != cudaSuccess ||
+        (err = h2d(a.counts, h.counts.data(), E * 4)) != cudaSuccess ||
+        (err = h2d(a.offsets, h.offsets.data(), (E + 1) * 4)) != cudaSuccess ||
+        (err = h2d(a.tiles, h.tiles.data(), h.tiles.size() * 4)) != cudaSuccess ||
+        (err = h2d(a.num_tiles, &h.num_tiles, 4)) != cudaSuccess ||
+        (err = h2d(a.ws + a.L.gu_tiles, h.gu.data(), h.gu.size() * 4)) != cudaSuccess ||
+        (err = h2d(a.ws + a.L.gu_num, &h.gu_num, 4)) != cudaSuccess ||
+        (err = h2d(a.ws + a.L.dn_tiles, h.dn.data(), h.dn.size() * 4)) != cudaSuccess ||
+        (err = h2d(a.ws + a.L.dn_num, &h.dn_num, 4)) != cudaSuccess)
+        return err;
+    // pageable sources: every copy above has consumed its source when it returns
+    *launches += 1;
     return launch_with_pdl(route_scatter, dim3(nblk, a.k), dim3(256), 0, st, a);
 }
 

@@ -109,6 +109,30 @@ def test_static_scratch_rejects_what_does_not_fit(lib):
     assert rc == _lib.MOE_ERR_UNSUPPORTED
 
 
+def test_host_routing_option_is_validated(lib):
+    """moe_options.host_routing takes 0 or 1; anything else is an argument error (no GPU)."""
+    s = _lib.moe_shape(512, 2048, 256, 8, 512, 512, 64)
+    for v, ok in ((0, True), (1, True), (2, False), (-1, False)):
+        o = _lib.moe_options(32, 1, 0, 0, v)
+        n = lib.moe_workspace_bytes(ctypes.byref(s), ctypes.byref(o))
+        assert (n > 0) == ok, (v, n)
+
+
+def test_unfused_dequant_option_sizes_the_workspace(lib):
+    """moe_options.unfused_dequant takes 0 or 1; with 1 the prefill workspace also holds every
+    expert's weights as bf16 ((E + 1) x 6 MB at d=2048, I=512), decode's does not (no GPU)."""
+    s = _lib.moe_shape(512, 2048, 256, 8, 512, 512, 64)
+    base = lib.moe_workspace_bytes(ctypes.byref(s), ctypes.byref(_lib.moe_options(32, 1, 0, 0, 0, 0)))
+    big = lib.moe_workspace_bytes(ctypes.byref(s), ctypes.byref(_lib.moe_options(32, 1, 0, 0, 0, 1)))
+    pairs = (512 // 128) * (2048 // 64) + (2048 // 256) * (512 // 64)
+    assert big >= base + 257 * pairs * 32768 and big < base + 257 * pairs * 32768 + 4096
+    for v in (2, -1):
+        assert lib.moe_workspace_bytes(ctypes.byref(s), ctypes.byref(_lib.moe_options(32, 1, 0, 0, 0, v))) == 0
+    s1 = _lib.moe_shape(1, 2048, 256, 8, 512, 512, 64)
+    assert (lib.moe_workspace_bytes(ctypes.byref(s1), ctypes.byref(_lib.moe_options(32, 1, 0, 0, 0, 1))) ==
+            lib.moe_workspace_bytes(ctypes.byref(s1), None))
+
+
 def test_deterministic_option_is_validated(lib):
     """moe_options.deterministic takes 0 or 1; anything else is an argument error (no GPU)."""
     s = _lib.moe_shape(4096, 2048, 256, 8, 512, 512, 64)

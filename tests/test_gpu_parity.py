@@ -259,3 +259,56 @@ def test_output_paths_and_deterministic_mode():
         assert_output_close(y_to_f64(y)[toks], out_ref, f"deterministic={det}")
         ys.setdefault(det, []).append(y.clone())
     assert torch.equal(ys[1][0], ys[1][1]), "deterministic mode: repeated calls differ"
+
+
+HOST_ROUTING = [
+    configs.custom_workload("skew_t333_d512_i128", T=333, d=512, I=128, seed=21, zipf_s=1.2),
+    configs.WORKLOADS["prefill_t512_d2048"],
+]
+
+
+@pytest.mark.parametrize("wl", HOST_ROUTING, ids=lambda w: w.name)
+def test_host_routing_ablation_matches_device_routing(wl):
+    """moe_options.host_routing = 1 (counts copied to the host, scan / block map / GEMM tile
+    lists computed there and copied back) reproduces the GPU-resident routing exactly: the
+    same routing outputs as the oracle and the same output bits (the fixed-order combine)."""
+    shp, lay, x, dl = _setup(wl)
+    xd = to_dev(x)
+    ref = oracle.route(x, lay.w_router, lay.logit_bias)
+    got = {}
+    for hr in (0, 1):
+        rt, ws, y = run_forward(shp, dl, xd, opts=moe.options(host_routing=hr))
+        r = routing_to_host(rt, shp.T)
+        assert_routing_equal(r, ref)
+        got[hr] = (r, y.clone())
+    for key in ("topk_idx", "topk_w", "counts", "offsets", "perm", "pos", "tiles"):
+        assert np.array_equal(got[0][0][key], got[1][0][key]), key
+    assert torch.equal(got[0][1], got[1][1]), "host-routing output bits differ from the device path"
+
+
+UNFUSED = [
+    configs.WORKLOADS["tiny_t128_d512"],
+    configs.custom_workload("skew_t333_d512_i128", T=333, d=512, I=128, seed=21, zipf_s=1.2),
+    configs.WORKLOADS["prefill_t512_d2048"],
+]
+
+
+@pytest.mark.parametrize("wl", UNFUSED, ids=lambda w: w.name)
+def test_unfused_dequant_ablation_matches_fused(wl):
+    """moe_options.unfused_dequant = 1 (every weight of a projection dequantised to bf16 in the
+    workspace by a separate kernel, then streamed by the GEMM) uses the same exact
+    dequantisation, so the output bits equal the fused path's; both match the oracle."""
+    shp, lay, x, dl = _setup(wl)
+    xd = to_dev(x)
+    ref = oracle.route(x, lay.w_router, lay.logit_bias)
+    toks = np.unique(np.concatenate([[0, shp.T - 1], np.random.default_rng(5).choice(shp.T, 10, replace=False)]))
+    toks = toks.astype(np.int32)
+    out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared, toks)
+    ys = {}
+    for uf in (0, 1):
+        opts = moe.options(unfused_dequant=uf)
+        rt, ws, y = run_forward(shp, dl, xd, opts=opts)
+        assert_routing_equal(routing_to_host(rt, shp.T), ref)
+        assert_output_close(y_to_f64(y)[toks], out_ref, f"unfused_dequant={uf}")
+        ys[uf] = y.clone()
+    assert torch.equal(ys[0], ys[1]), "unfused-dequant output bits differ from the fused path"
