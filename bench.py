@@ -7,9 +7,10 @@ synthetic input of the workload.  Default workload: the 512-token prefill chunk 
 256 experts, top-8, I=512 + shared expert), whose 455 MB of 4-bit weights exceed L2, so every
 step streams its inputs from HBM (a workload whose layer fits in L2 rotates through enough
 independent layer copies to exceed it).  Timing: W untimed steps, then K steps between CUDA events on
-the launching stream (each step is replayed from a CUDA graph of the library calls; every 8th
-step replays one graph per phase instead, with events between the phases that give the
-gate/up and down kernel times), barrier + synchronize on both sides, max over ranks.  Multi-GPU (torchrun): every rank runs its own
+the launching stream (prefill steps are replayed 8 at a time from one CUDA graph of the library
+calls; every 8th such chunk runs its steps from one graph per phase instead, with events between
+the phases that give the gate/up and down kernel times; K is rounded up to a multiple of 8),
+barrier + synchronize on both sides, max over ranks.  Multi-GPU (torchrun): every rank runs its own
 chunks (weak scaling, no collective on the data path).
 
 --impl reference times the CPU oracle on bounded samples of the same workload on the host
@@ -214,9 +215,10 @@ def run_ours(args, rank, world, local):
                 for f in calls_for(L[gi % layers], xs[gi % len(xs)]).values():
                     f()
             stream.synchronize()
-            # per set: the whole step as one graph (consecutive kernels overlap their prologues
-            # through programmatic dependent launch) and the four phases as separate graphs, which
-            # every PROBE-th timed step runs instead, with events between them for the kernel times
+            # per set: the four phases as separate graphs (probe chunks, below, run these with
+            # events between them for the kernel times); and MULTI consecutive steps (a multiple
+            # of the set count) as one graph, in which consecutive kernels, also across steps,
+            # overlap their prologues through programmatic dependent launch
             graphs = []
             for gi in range(nsets):
                 if gi == 0:
@@ -230,25 +232,27 @@ def run_ours(args, rank, world, local):
                     gc[name] = g
                 if gi == 0:
                     launches_one_chunk = moe.moe_launch_count() - n0
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    for f in calls.values():
-                        f()
-                gc["step"] = g
                 graphs.append(gc)
+            MULTI = nsets * -(-8 // nsets)
+            multi = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(multi, stream=stream):
+                for s in range(MULTI):
+                    for f in calls_for(L[s % layers], xs[s % len(xs)]).values():
+                        f()
     launches_per_step = moe.moe_launch_count() - n0 if decode else launches_one_chunk
     torch.cuda.synchronize()
 
-    # prefill: a step runs the graphs of its chunk, which read the chunk where it resides;
+    # prefill: steps run in chunks of MULTI (one graph replay; each step reads its chunk where it
+    # resides); every PROBE-th chunk runs its steps phase by phase with events in between.
     # decode: a step copies its token's activations (4 KB) into the graph's input buffer first
     PROBE = 8
+    if decode:
+        MULTI = 1
 
     def step(s, ev=None):
         if decode:
             x_in.copy_(x_all[s % nsteps_x:s % nsteps_x + 1], non_blocking=True)
             graphs["step"].replay()
-        elif ev is None:
-            graphs[s % len(graphs)]["step"].replay()
         else:
             gc = graphs[s % len(graphs)]
             gc["route"].replay()
@@ -262,27 +266,44 @@ def run_ours(args, rank, world, local):
                 ev[2].record(stream)
             gc["combine"].replay()
 
+    def chunk(c, evs=None):
+        """Steps c*MULTI .. c*MULTI + MULTI - 1."""
+        if decode:
+            step(c)
+        elif evs is None:
+            multi.replay()
+        else:
+            for j in range(MULTI):
+                step(c * MULTI + j, evs[j])
+
     dist = None
     if world > 1:
         import torch.distributed as dist
     with torch.cuda.stream(stream):
-        for s in range(args.warmup):
-            step(s)
+        nwarm = -(-args.warmup // MULTI)
+        for c in range(nwarm):
+            chunk(c)
+        if not decode:   # the phase graphs too
+            chunk(0, [None] * MULTI)
         stream.synchronize()
+        warmup_steps = nwarm * MULTI + (0 if decode else MULTI)
         # auto step count: about 1.5 s of timed work
         if args.steps is None:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = max(1, 24 // MULTI)
             e0.record(stream)
-            for s in range(20):
-                step(s)
+            for c in range(n):
+                chunk(c)
             e1.record(stream)
             e1.synchronize()
-            per = e0.elapsed_time(e1) / 20
+            per = e0.elapsed_time(e1) / (n * MULTI)
             K = int(min(20000, max(20, 1500.0 / max(per, 1e-3))))
         else:
             K = args.steps
-        evs = {s: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for s in range(0, K, PROBE)} \
-            if not decode else {}
+        nchunks = -(-K // MULTI)
+        K = nchunks * MULTI
+        evs = {c: [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(MULTI)]
+               for c in range(0, nchunks, PROBE)} if not decode else {}
         clocks = ClockSampler(local)
         clocks.start()
         time.sleep(0.15)
@@ -292,8 +313,8 @@ def run_ours(args, rank, world, local):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for s in range(K):
-            step(s, evs.get(s))
+        for c in range(nchunks):
+            chunk(c, evs.get(c))
         t1.record(stream)
         t1.synchronize()
         torch.cuda.synchronize()
@@ -310,7 +331,7 @@ def run_ours(args, rank, world, local):
     assert rc == moe.MOE_OK, f"device status {rc} bits {bits}"
 
     P = peaks()
-    res = dict(metric=METRIC, n_gpus=world, steps=K, warmup=args.warmup, ms_per_step=ms_step, data="synthetic",
+    res = dict(metric=METRIC, n_gpus=world, steps=K, warmup=warmup_steps, ms_per_step=ms_step, data="synthetic",
                scaling="weak", vs_baseline=None, dtype="bf16", clocks=clk,
                gpu_launches=int(launches_per_step * K))
     if decode:
@@ -329,7 +350,7 @@ def run_ours(args, rank, world, local):
     else:
         value = world * T * K / (ms_total / 1000.0)
         res.update(value=value, unit="routed tokens/s", higher_is_better=True)
-        ph = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in evs.values()])
+        ph = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for ce in evs.values() for e in ce])
         gu_ms, dn_ms = float(ph[:, 0].mean()), float(ph[:, 1].mean())
         counts = rt.counts.cpu().numpy()
         A = algorithmic_counts(shp, counts)
