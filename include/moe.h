@@ -174,6 +174,15 @@ int moe_route(const moe_shape* shape, const uint16_t* x_dev, const uint16_t* w_r
               const float* logit_bias_dev, const moe_routing* routing, void* workspace_dev,
               size_t workspace_bytes, const moe_options* options, void* stream);
 
+/* Step a1 on its own: every router logit of every token, exactly as moe_route defines them
+ * (the fixed fp32 order above, then + logit_bias[e]), computed by the same device code that
+ * moe_route uses for its exact recomputation.  logits_dev: fp32 [T][E], caller-owned, written
+ * asynchronously on stream.  x_dev and w_router_dev 16-byte aligned, logit_bias_dev (nullable)
+ * 4-byte aligned, logits_dev 16-byte aligned; no workspace.  For inspection and tests: moe_route
+ * itself does not materialise all logits. */
+int moe_router_logits(const moe_shape* shape, const uint16_t* x_dev, const uint16_t* w_router_dev,
+                      const float* logit_bias_dev, float* logits_dev, void* stream);
+
 /* Steps a7-a9: for every expert group and the shared expert, gate/up projections with
  * SwiGLU (h kept to 16 bits as a bf16 pair), output projection, and the fp32 weighting
  * (routing weight topk_w for routed rows, 1 for the shared expert).  Prefill writes every

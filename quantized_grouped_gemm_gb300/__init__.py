@@ -143,6 +143,12 @@ def moe_route(shp, x, w_router, logit_bias, routing: Routing, ws, opts=None, str
                            ws.numel(), _o(opts), _s(stream)), "moe_route")
 
 
+def moe_router_logits(shp, x, w_router, logit_bias, out, stream=None) -> None:
+    """Every exact router logit (fp32 [T][E] into out), as moe_route defines them."""
+    _check(lib().moe_router_logits(ctypes.byref(shp), _p(x), _p(w_router), _p(logit_bias), _p(out), _s(stream)),
+           "moe_router_logits")
+
+
 def moe_ffn_gate_up(shp, x, routing: Routing, packed_routed, packed_shared, ws, opts=None, stream=None) -> None:
     _check(lib().moe_ffn_gate_up(ctypes.byref(shp), _p(x), routing.ref(), _p(packed_routed), _p(packed_shared),
                                  _p(ws), ws.numel(), _o(opts), _s(stream)), "moe_ffn_gate_up")

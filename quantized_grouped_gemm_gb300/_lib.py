@@ -59,6 +59,7 @@ _SIG = {
                                         ctypes.c_size_t, _P]),
     "moe_route": (ctypes.c_int, [_SPS, _P, _P, _P, ctypes.POINTER(moe_routing), _P, ctypes.c_size_t,
                                  ctypes.POINTER(moe_options), _P]),
+    "moe_router_logits": (ctypes.c_int, [_SPS, _P, _P, _P, _P, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_SPS, _P, ctypes.POINTER(moe_routing), _P, _P, _P, ctypes.c_size_t,
                                        ctypes.POINTER(moe_options), _P]),
     "moe_ffn_gate_up": (ctypes.c_int, [_SPS, _P, ctypes.POINTER(moe_routing), _P, _P, _P, ctypes.c_size_t,

@@ -248,6 +248,20 @@ static int route_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_r
     return cuda_status(e);
 }
 
+int moe_router_logits(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
+                      float* logits, void* stream) {
+    int rc = moe_check_shape(s);
+    if (rc != MOE_OK) return rc;
+    if (s->T == 0) return MOE_OK;
+    if (!x || !w_router || !logits || !aligned(x, 16) || !aligned(w_router, 16) || !aligned(logits, 16) ||
+        (bias && !aligned(bias, 4)))
+        return MOE_ERR_INVALID_ARG;
+    unsigned long long n = 0;
+    const cudaError_t e = launch_router_logits(x, w_router, bias, logits, s->T, s->d, static_cast<cudaStream_t>(stream), &n);
+    g_launches += n;
+    return cuda_status(e);
+}
+
 int moe_route(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
               const moe_routing* rt, void* ws, size_t ws_bytes, const moe_options* o, void* stream) {
     return route_impl(s, x, w_router, bias, rt, ws, ws_bytes, o, stream, nullptr);

@@ -643,6 +643,8 @@ struct FfnArgs {
 
 cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_route_prefill_host(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);
+cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w_router, const float* bias, float* out, int T,
+                                 int d, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_route_decode(const RouteArgs& a, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_combine(int T, int d, const float* acc, uint16_t* y, cudaStream_t st, unsigned long long* launches);
 cudaError_t launch_decode_gate_up(const FfnArgs& a, cudaStream_t st, unsigned long long* launches);

@@ -201,6 +201,13 @@ __global__ void __launch_bounds__(192, 1)
 // are recomputed.  The result equals top-8 over all 256 exact logits.
 // Also writes the block's per-expert counts.
 // ---------------------------------------------------------------------------------------
+// p = fma(x.lo, w.lo, p), then p = fma(x.hi, w.hi, p), for the bf16 halves of two 32-bit words
+// (bf16 -> fp32 is exact, so each step rounds once)
+__device__ __forceinline__ float fma2_bf16(uint32_t x, uint32_t w, float p) {
+    p = fmaf(bf16lo(x), bf16lo(w), p);
+    return fmaf(bf16hi(x), bf16hi(w), p);
+}
+
 // Exact logits (fixed order, as warp_pinned_logit) of G experts for the token row held in
 // registers, with all G rows' loads issued before the arithmetic.
 template <int NI, int G>
@@ -218,14 +225,10 @@ __device__ __forceinline__ void warp_pinned_logits(const uint4 (&xv)[8], const u
     for (int i = 0; i < NI; ++i) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            p[g] = fmaf(bf16lo(xv[i].x), bf16lo(a[g][i].x), p[g]);
-            p[g] = fmaf(bf16hi(xv[i].x), bf16hi(a[g][i].x), p[g]);
-            p[g] = fmaf(bf16lo(xv[i].y), bf16lo(a[g][i].y), p[g]);
-            p[g] = fmaf(bf16hi(xv[i].y), bf16hi(a[g][i].y), p[g]);
-            p[g] = fmaf(bf16lo(xv[i].z), bf16lo(a[g][i].z), p[g]);
-            p[g] = fmaf(bf16hi(xv[i].z), bf16hi(a[g][i].z), p[g]);
-            p[g] = fmaf(bf16lo(xv[i].w), bf16lo(a[g][i].w), p[g]);
-            p[g] = fmaf(bf16hi(xv[i].w), bf16hi(a[g][i].w), p[g]);
+            p[g] = fma2_bf16(xv[i].x, a[g][i].x, p[g]);
+            p[g] = fma2_bf16(xv[i].y, a[g][i].y, p[g]);
+            p[g] = fma2_bf16(xv[i].z, a[g][i].z, p[g]);
+            p[g] = fma2_bf16(xv[i].w, a[g][i].w, p[g]);
         }
     }
 #pragma unroll
@@ -832,6 +835,47 @@ cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned l
         return err;
     if ((err = launch_with_pdl(route_scan, dim3(1), dim3(1024), 0, st, a)) != cudaSuccess) return err;
     return launch_with_pdl(route_scatter, dim3(nblk, a.k), dim3(256), 0, st, a);
+}
+
+namespace {
+// ---------------------------------------------------------------------------------------
+// router_logits_exact: every logit of every token with the exact recomputation's device code
+// (pinned_logit_group, kCertGroup experts per round); one warp per (token, 32 experts).
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) router_logits_exact(const uint16_t* __restrict__ x,
+                                                           const uint16_t* __restrict__ w_router,
+                                                           const float* __restrict__ bias, float* __restrict__ out,
+                                                           int T, int d) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);   // (token, expert group of 32)
+    const int t = gw >> 3, e0 = (gw & 7) * 32;
+    if (t >= T) return;
+    const uint16_t* xrow = x + (size_t)t * d;
+    uint4 xv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        xv[i] = make_uint4(0, 0, 0, 0);
+        if (i < d / 256) xv[i] = ld_nc_v4(xrow + 256 * i + 8 * lane);
+    }
+    for (int g0 = 0; g0 < 32; g0 += kCertGroup) {
+        int eg[kCertGroup];
+#pragma unroll
+        for (int g = 0; g < kCertGroup; ++g) eg[g] = e0 + g0 + g;
+        float lg[kCertGroup];
+        pinned_logit_group<kCertGroup>(xv, xrow, w_router, d, eg, lane, lg);
+#pragma unroll
+        for (int g = 0; g < kCertGroup; ++g)
+            if (lane == g0 + g) out[(size_t)t * 256 + eg[g]] = bias ? lg[g] + bias[eg[g]] : lg[g];
+    }
+}
+}  // namespace
+
+cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w_router, const float* bias, float* out, int T,
+                                 int d, cudaStream_t st, unsigned long long* launches) {
+    *launches += 1;
+    return launch_with_pdl(router_logits_exact, dim3((unsigned)T), dim3(256), 0, st, x, w_router, bias, out, T, d);
 }
 
 // ---------------------------------------------------------------------------------------

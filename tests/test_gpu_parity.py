@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import quantized_grouped_gemm_gb300 as moe
-from moe_workload import configs
+from moe_workload import configs, gen
 from gpu_helpers import (DeviceLayer, assert_output_close, assert_routing_equal, routing_to_host, run_forward,
                          to_dev, y_to_f64)
 
@@ -312,3 +312,57 @@ def test_unfused_dequant_ablation_matches_fused(wl):
         assert_output_close(y_to_f64(y)[toks], out_ref, f"unfused_dequant={uf}")
         ys[uf] = y.clone()
     assert torch.equal(ys[0], ys[1]), "unfused-dequant output bits differ from the fused path"
+
+
+def _adversarial_router(T, d, seed):
+    """bf16 rows whose products span fp32's range: exponents from -75 to +40 (subnormal
+    products and subnormal bf16 inputs included), random signs, some exact zeros."""
+    rng = np.random.default_rng(seed)
+    def rows(n):
+        m = rng.uniform(1.0, 2.0, (n, d)) * rng.choice([-1.0, 1.0], (n, d))
+        e = rng.integers(-75, 41, (n, d)).astype(np.float64)
+        v = m * np.exp2(e)
+        v[rng.random((n, d)) < 0.02] = 0.0
+        sub = rng.random((n, d)) < 0.01                      # bf16 subnormals (below 2^-126)
+        v[sub] = rng.uniform(-1, 1, sub.sum()) * 2.0 ** -127
+        return gen.f32_to_bf16_bits(v.astype(np.float32))
+    return rows(T), rows(256)
+
+
+ROUTER_LOGIT_CASES = [
+    ("tiny_t128_d512", None),
+    ("prefill_t512_d2048", 64),
+    ("d768", None),
+    ("adversarial_d2048", None),
+    ("adversarial_d768", None),
+]
+
+
+@pytest.mark.parametrize("case,rows", ROUTER_LOGIT_CASES, ids=[c[0] for c in ROUTER_LOGIT_CASES])
+def test_router_logits_bit_exact(case, rows):
+    """moe_router_logits (the device code of the exact recomputation) equals the oracle's fixed
+    fp32 order bit for bit, with and without a logit bias, for ordinary router inputs and for
+    rows whose products cover subnormal to large magnitudes; d = 768 takes the generic loop."""
+    if case.startswith("adversarial"):
+        d = int(case.split("_d")[1])
+        x, wr = _adversarial_router(96, d, seed=d)
+    elif case == "d768":
+        wl = configs.custom_workload("t40_d768_i128", T=40, d=768, I=128, seed=17)
+        lay = configs.make_layer(wl)
+        x, wr = configs.make_x(wl), lay.w_router
+    else:
+        wl = configs.WORKLOADS[case]
+        lay = configs.make_layer(wl)
+        x, wr = configs.make_x(wl), lay.w_router
+    if rows is not None:
+        x = x[:rows]
+    T, d = x.shape
+    shp = moe.shape(T, d, 256, 8, 128, 128)
+    bias = np.random.default_rng(T + d).normal(0.0, 0.5, 256).astype(np.float32)
+    for b in (None, bias):
+        out = torch.empty(T, 256, dtype=torch.float32, device="cuda")
+        moe.moe_router_logits(shp, to_dev(x), to_dev(wr), None if b is None else to_dev(b), out)
+        got = out.cpu().numpy()
+        ref = oracle.router_logits(x, wr, b)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), \
+            f"{case} bias={b is not None}: {(got.view(np.uint32) != ref.view(np.uint32)).sum()} logits differ"
