@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablations", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="decode: layer copies (default: the workload's); fewer for small profiling captures")
     ap.add_argument("--cpu-sample-tokens", type=int, default=32)
     return ap.parse_args()
 
@@ -150,7 +152,7 @@ def run_ours(args, rank, world, local):
     layer_bytes = sum(n * (3 * sh.d * i // 2 + 3 * sh.d * i // 16) for n, i in ((sh.E, sh.I), (1, sh.I_shared)))
     # a step's weights must not sit in L2 between steps: a workload whose layer fits rotates
     # through enough independent layer copies to exceed twice the L2 size
-    layers = wl.layers if decode else max(1, -(-2 * L2_BYTES // layer_bytes))
+    layers = (args.layers or wl.layers) if decode else max(1, -(-2 * L2_BYTES // layer_bytes))
 
     def to_dev(a):
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a)).to(dev)
