@@ -119,6 +119,15 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------- work
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the roofline kernel,
+# from an ncu full capture of the current kernels on each workload (None: not captured)
+TRAFFIC_BYTES = {
+    "prefill_t512_d2048": 322.282240e6 + 9.842176e6,     # ffn_tm_kernel<0, 0> (gate/up)
+    "prefill_t4096_d2048": 454.402304e6 + 61.936384e6,   # ffn_tm_kernel<0, 0> (gate/up)
+    "decode_t1_d2048": 17.082624e6,                       # decode_fused, one layer
+}
+
+
 def algorithmic_counts(shp, counts):
     """Per-launch algorithmic bytes and FLOPs of the gate/up and down kernels (real rows only)."""
     T, d, I = shp.T, shp.d, shp.I
@@ -343,7 +352,7 @@ def run_ours(args, rank, world, local):
         bytes_layer = sh.E * sh.d * 2 + 9 * (3 * sh.d * sh.I // 2 + 3 * sh.d * sh.I // 64 * 4)
         gbs = bytes_layer / (us_tok_layer * 1e-6) / 1e9
         res["roofline"] = dict(bound="hbm", achieved=gbs, peak=P["hbm_gbs"], unit="GB/s", frac=gbs / P["hbm_gbs"],
-                               traffic=None, kernel="decode_fused (one launch per layer: route + gate/up + down + combine)",
+                               traffic=TRAFFIC_BYTES.get(wl.name), kernel="decode_fused (one launch per layer: route + gate/up + down + combine)",
                                bytes_per_token_layer=bytes_layer, peak_source=P["source"])
         res["config"] = dict(workload=wl.name, T=1, d=sh.d, E=sh.E, k=sh.k, I=sh.I, I_shared=sh.I_shared,
                              layers=layers, l2=f"inputs larger than L2: {layers} layer copies of the weights, "
@@ -365,7 +374,7 @@ def run_ours(args, rank, world, local):
         else:
             ach = A["gu_flops"] / (gu_ms * 1e-3) / 1e12
             roof = dict(bound="tensor", achieved=ach, peak=P["bf16_tflops"], unit="TFLOP/s", frac=ach / P["bf16_tflops"])
-        roof.update(traffic=None, kernel="ffn_tm_kernel<0> (gate/up + SwiGLU; tcgen05, dequantised weights in TMEM)", algorithmic_bytes=A["gu_bytes"],
+        roof.update(traffic=TRAFFIC_BYTES.get(wl.name), kernel="ffn_tm_kernel<0> (gate/up + SwiGLU; tcgen05, dequantised weights in TMEM)", algorithmic_bytes=A["gu_bytes"],
                     algorithmic_flops=A["gu_flops"], kernel_ms=gu_ms, peak_source=P["source"])
         res["roofline"] = roof
         ffn_ms = gu_ms + dn_ms
