@@ -56,6 +56,23 @@ def dist_env():
     return rank, world, local
 
 
+def rank_rotation(items, rank):
+    """Weak scaling: rank r takes the chunks starting at its own offset r (mod the chunk count)."""
+    k = rank % len(items)
+    return items[k:] + items[:k]
+
+
+def max_over_ranks(x, dist=None):
+    """The slowest rank's value (a host-tensor all-reduce over the process group; the data path
+    itself has no collective)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -187,7 +204,7 @@ def run_ours(args, rank, world, local):
         xs = [to_dev(np.ascontiguousarray(x_full[c * T:(c + 1) * T])) for c in range(nchunk)]
         del x_full
         if world > 1:      # weak scaling: each rank its own rotation of the chunks
-            xs = xs[rank % len(xs):] + xs[:rank % len(xs)]
+            xs = rank_rotation(xs, rank)
     rt = moe.Routing(T)
     ws = moe.workspace(shp)
     y = torch.empty(T, sh.d, dtype=torch.int16, device=dev)
@@ -332,11 +349,7 @@ def run_ours(args, rank, world, local):
         if dist is not None:
             dist.barrier()
         clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    if dist is not None:
-        tt = torch.tensor([ms_total], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dist)
     ms_step = ms_total / K
     rc, bits = moe.moe_read_status(ws, stream)
     assert rc == moe.MOE_OK, f"device status {rc} bits {bits}"
