@@ -366,3 +366,30 @@ def test_router_logits_bit_exact(case, rows):
         ref = oracle.router_logits(x, wr, b)
         assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), \
             f"{case} bias={b is not None}: {(got.view(np.uint32) != ref.view(np.uint32)).sum()} logits differ"
+
+
+MAX_SHAPES = [
+    configs.custom_workload("max_t65536_d256_i128", T=65536, d=256, I=128, seed=31),
+    configs.custom_workload("max_t64_d7168_i128", T=64, d=7168, I=128, seed=32),
+    configs.custom_workload("max_t64_d256_i8192", T=64, d=256, I=8192, seed=33),
+]
+
+
+@pytest.mark.parametrize("wl", MAX_SHAPES, ids=lambda w: w.name)
+def test_maximum_sizes(wl):
+    """Each largest supported dimension (T = 65536, d = 7168, I = 8192) with the others small:
+    routing bit-exact, sampled outputs within tolerance, deterministic mode included for the
+    row path."""
+    shp, lay, x, dl = _setup(wl)
+    xd = to_dev(x)
+    ref = oracle.route(x, lay.w_router, lay.logit_bias)
+    T = shp.T
+    toks = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(7).choice(T, 14, replace=False)]))
+    toks = toks.astype(np.int32)
+    out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared, toks)
+    for det in (0, 1):
+        rt, ws, y = run_forward(shp, dl, xd, opts=moe.options(deterministic=det))
+        assert_routing_equal(routing_to_host(rt, T), ref)
+        assert_output_close(y_to_f64(y)[toks], out_ref, f"{wl.name} deterministic={det}")
+        del rt, ws, y
+        torch.cuda.empty_cache()
