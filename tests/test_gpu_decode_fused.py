@@ -153,3 +153,17 @@ def test_gemv_decode_path_on_request():
         assert _forward(shp, dl, to_dev(x), rt, ws, y, moe.options(decode_path=path)) == launches
         assert moe.moe_read_status(ws)[0] == moe.MOE_OK
         _check(x, lay, rt, y, f"I=384 path {path}")
+
+
+def test_decode_largest_intermediate_falls_back_to_gemv():
+    """I = 8192 (the largest supported): the one-launch kernel's grid (9 slots x 64 h slices)
+    cannot be resident at once, so moe_forward runs the three decode kernels; routing exact,
+    output within tolerance."""
+    wl, lay, shp, dl = _layer("fz_d256_i8192", 256, 8192, seed=9)
+    x = configs.make_decode_x(wl, 1)
+    rt, ws = moe.Routing(1), moe.workspace(shp)
+    y = torch.empty(1, 256, dtype=torch.int16, device="cuda")
+    n = _forward(shp, dl, to_dev(x), rt, ws, y)
+    assert moe.moe_read_status(ws)[0] == moe.MOE_OK
+    assert n == 3, f"expected the three decode kernels, got {n} launches"
+    _check(x, lay, rt, y, "decode d=256 I=8192")
