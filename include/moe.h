@@ -112,11 +112,11 @@ typedef struct moe_options {
     int tile_rows;          /* rows per exported block-map tile; default 32 */
     int decode_max_tokens;  /* T at or below this runs the decode (GEMV) kernels; default 1 */
     int decode_path;        /* MOE_DECODE_AUTO (default) or MOE_DECODE_GEMV */
-    int deterministic;      /* 0 (default): prefill sums each token's weighted rows in a fixed order
-                               when they fit well inside L2 ((k+1)*T*d*4 bytes <= 64 MB) and adds
-                               them into the fp32 sum with bulk reduce-adds otherwise (addition
-                               order not fixed); 1: always the fixed order, so repeated calls give
-                               identical bits (the rows then pass through HBM at large T) */
+    int deterministic;      /* 0 (default): prefill adds each token's weighted rows into an fp32
+                               sum with bulk reduce-adds (addition order not fixed, so the last
+                               bits may differ between calls); 1: the rows are stored and summed
+                               per token in a fixed order, so repeated calls give identical bits
+                               (slower: the rows make a round trip through L2, or HBM at large T) */
     int host_routing;       /* 0 (default): the routing scan and block map stay on the GPU.
                                1: an ablation of that design ("GPU-resident routing" on the
                                page): moe_route copies the per-block expert counts to the host,

@@ -240,10 +240,10 @@ def test_default_scales_use_the_denormal_encoding():
 
 
 def test_output_paths_and_deterministic_mode():
-    """A 1024-token chunk: its weighted rows (9 x 1024 x 2048 fp32 = 75 MB) exceed what the
-    default keeps in L2, so the down projection adds into the fp32 sum; deterministic = 1 takes
-    the rows path with the fixed-order combine.  Both match the oracle (sampled tokens), and the
-    deterministic mode gives identical bits on a repeated call."""
+    """A 1024-token chunk: by default the down projection adds its weighted rows into the fp32
+    sum; deterministic = 1 stores the rows (9 x 1024 x 2048 fp32 = 75 MB) and sums them in a
+    fixed order.  Both match the oracle (sampled tokens), and the deterministic mode gives
+    identical bits on a repeated call."""
     wl = configs.custom_workload("t1024_d2048_i512", T=1024, d=2048, I=512, seed=11)
     shp, lay, x, dl = _setup(wl)
     xd = to_dev(x)
@@ -271,13 +271,13 @@ HOST_ROUTING = [
 def test_host_routing_ablation_matches_device_routing(wl):
     """moe_options.host_routing = 1 (counts copied to the host, scan / block map / GEMM tile
     lists computed there and copied back) reproduces the GPU-resident routing exactly: the
-    same routing outputs as the oracle and the same output bits (the fixed-order combine)."""
+    same routing outputs as the oracle and the same output bits (deterministic mode)."""
     shp, lay, x, dl = _setup(wl)
     xd = to_dev(x)
     ref = oracle.route(x, lay.w_router, lay.logit_bias)
     got = {}
     for hr in (0, 1):
-        rt, ws, y = run_forward(shp, dl, xd, opts=moe.options(host_routing=hr))
+        rt, ws, y = run_forward(shp, dl, xd, opts=moe.options(host_routing=hr, deterministic=1))
         r = routing_to_host(rt, shp.T)
         assert_routing_equal(r, ref)
         got[hr] = (r, y.clone())
@@ -297,7 +297,8 @@ UNFUSED = [
 def test_unfused_dequant_ablation_matches_fused(wl):
     """moe_options.unfused_dequant = 1 (every weight of a projection dequantised to bf16 in the
     workspace by a separate kernel, then streamed by the GEMM) uses the same exact
-    dequantisation, so the output bits equal the fused path's; both match the oracle."""
+    dequantisation, so in deterministic mode the output bits equal the fused path's; both
+    match the oracle."""
     shp, lay, x, dl = _setup(wl)
     xd = to_dev(x)
     ref = oracle.route(x, lay.w_router, lay.logit_bias)
@@ -306,7 +307,7 @@ def test_unfused_dequant_ablation_matches_fused(wl):
     out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared, toks)
     ys = {}
     for uf in (0, 1):
-        opts = moe.options(unfused_dequant=uf)
+        opts = moe.options(unfused_dequant=uf, deterministic=1)
         rt, ws, y = run_forward(shp, dl, xd, opts=opts)
         assert_routing_equal(routing_to_host(rt, shp.T), ref)
         assert_output_close(y_to_f64(y)[toks], out_ref, f"unfused_dequant={uf}")
