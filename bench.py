@@ -139,7 +139,7 @@ class ClockSampler:
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the roofline kernel,
 # from an ncu full capture of the current kernels on each workload (None: not captured)
 TRAFFIC_BYTES = {
-    "prefill_t512_d2048": 322.282240e6 + 9.842176e6,     # ffn_tm_kernel<0, 0> (gate/up)
+    "prefill_t512_d2048": 322.273536e6 + 9.660928e6,     # ffn_tm_kernel<0, 0> (gate/up)
     "prefill_t4096_d2048": 454.402304e6 + 61.936384e6,   # ffn_tm_kernel<0, 0> (gate/up)
     "decode_t1_d2048": 17.082624e6,                       # decode_fused, one layer
 }
