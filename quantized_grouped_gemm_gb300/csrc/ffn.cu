@@ -93,11 +93,13 @@ struct TmCfg {
     static constexpr int RX = kDown ? (kBf16 ? 2 : 4) : 8;   // token-row ring slots
     static constexpr int CH = kBf16 ? kBf16PairBytes : kChunkPairBytes;   // bytes of a weight chunk
     static constexpr int RC = kBf16 ? (kDown ? 4 : 2) : (kDown ? 6 : 8);  // weight-chunk ring slots
-    // The two dequant sets take alternate K blocks, so with an even ring every slot belongs to
+    // The two dequant sets take alternate K blocks.  With an even ring every slot belongs to
     // one set, whose parity waits on it are then never more than one phase ahead.  With an odd
-    // ring a set can reach a slot's next parity wait while the other set's block is still
-    // pending there; the wait then passes at once and the ring's barriers fall out of step.
-    static_assert(RC % 2 == 0, "weight-chunk ring slots must come in pairs, one per dequant set");
+    // ring consecutive uses of a slot alternate between the sets: a set reaching block it has
+    // finished block it - 2, which waited for block it - 2 - A, so the slot's previous block
+    // it - RC is certain to be done only when RC >= A + 2.  A smaller odd ring lets a parity wait
+    // pass a phase early, and the ring's barriers fall out of step.
+    static_assert(RC % 2 == 0 || RC >= A + 2, "weight-chunk ring: even, or at least A + 2 slots");
     static constexpr int PARTS = kDown ? 2 : 1;              // hi, lo halves of h
     static constexpr int XS = PARTS * kTmXBytes;             // bytes of a token-row slot
     // staging of 32 tokens: gate/up bf16 [32][hi 128 | lo 128]; down two buffers of fp32 [32][128]
