@@ -121,6 +121,7 @@ static RouteArgs route_args(const moe_shape* s, const uint16_t* x, const uint16_
     a.num_tiles = rt->num_tiles_dev;
     a.ws = static_cast<uint8_t*>(ws);
     a.L = ws_layout(*s);
+    a.num_sms = num_sms();
     return a;
 }
 

@@ -619,7 +619,19 @@ struct RouteArgs {
     WsLayout L;
     const uint8_t* pf_ptr;     // optional: weights to warm in L2 while routing (decode)
     size_t pf_bytes;
+    int num_sms;               // grid of the persistent FFN kernels (tile j runs on CTA j % num_sms)
 };
+
+// Where the shared expert's tiles go in a GEMM tile list of `total` entries (`shared` of them):
+// the persistent kernels give entry j to CTA j % grid, so the CTAs from total % grid on run
+// one tile fewer; the shared expert's tiles (the chunk's full token blocks, the heaviest) are
+// placed at entry total % grid when they fit before the end of that round and of the list,
+// else first.  The experts' entries keep their order around them (a permutation of 0..total-1).
+__host__ __device__ inline int shared_tiles_at(int total, int shared, int grid) {
+    if (grid <= 0) return 0;
+    const int p0 = total % grid;
+    return p0 + shared <= grid && p0 + shared <= total ? p0 : 0;
+}
 
 struct FfnArgs {
     int T, d, E, k, I;

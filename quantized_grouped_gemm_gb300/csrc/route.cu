@@ -576,7 +576,9 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     // GEMM tile lists: an expert's rows split into near-equal token blocks (gate/up: at most
     // kGuRows rows; down: at most kDnRows); each block is repeated for every weight tile (weight
     // tile innermost, so the CTAs that run at the same time share the block's activation rows
-    // in L2).  The shared expert (expert index E) comes first and covers token rows 0..T-1.
+    // in L2).  The shared expert (expert index E) covers token rows 0..T-1 in full blocks; its
+    // tiles are inserted where the CTAs run one tile fewer (shared_tiles_at), the experts'
+    // tiles follow in expert order around them.
     const int MTgu = a.I / kTileRows, MTdn = a.d / 256;   // 128 gate+up row pairs; 256-row down tiles
     const int nn = (run + kGuRows - 1) / kGuRows;
     const int nd = (run + kDnRows - 1) / kDnRows;
@@ -590,25 +592,32 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     named_bar_sync(1, 256);
     int4* gu = reinterpret_cast<int4*>(a.ws + a.L.gu_tiles);
     int4* dn = reinterpret_cast<int4*>(a.ws + a.L.dn_tiles);
-    // nb near-equal blocks of `rows` rows from r0; block i goes to list slot base + i
-    auto split = [&](int4* list, int mt, int base, int ex, int r0, int rows, int nb) {
+    // nb near-equal blocks of `rows` rows from r0; entry j of block i (entry (base + i) * mt + m
+    // of its own sequence) goes to list position j + (j >= from ? by : 0)
+    auto split = [&](int4* list, int mt, int base, int ex, int r0, int rows, int nb, int from, int by) {
         const int q = rows / nb, rem = rows % nb;
         for (int i = 0; i < nb; ++i) {
             const int n = q + (i < rem ? 1 : 0);
-            for (int m = 0; m < mt; ++m) list[(size_t)(base + i) * mt + m] = make_int4(ex, r0, n, m);
+            for (int m = 0; m < mt; ++m) {
+                const int j = (base + i) * mt + m;
+                list[(size_t)(j >= from ? j + by : j)] = make_int4(ex, r0, n, m);
+            }
             r0 += n;
         }
     };
-    if (nn > 0) split(gu, MTgu, nsh + nbase, e, off, run, nn);
-    if (nd > 0) split(dn, MTdn, nshd + dbase, e, off, run, nd);
+    const int shg = nsh * MTgu, shd = nshd * MTdn;   // the shared expert's entries
+    const int pg = shared_tiles_at((nsh + s_tot[1]) * MTgu, shg, a.num_sms);
+    const int pd = shared_tiles_at((nshd + s_tot[2]) * MTdn, shd, a.num_sms);
+    if (nn > 0) split(gu, MTgu, nbase, e, off, run, nn, pg, shg);
+    if (nd > 0) split(dn, MTdn, dbase, e, off, run, nd, pd, shd);
     // shared expert token blocks (one thread each)
     for (int i = e; i < nsh; i += E) {
         const int q = a.T / nsh, rem = a.T % nsh;
-        split(gu, MTgu, i, E, i * q + min(i, rem), q + (i < rem ? 1 : 0), 1);
+        split(gu, MTgu, i, E, i * q + min(i, rem), q + (i < rem ? 1 : 0), 1, 0, pg);
     }
     for (int i = e; i < nshd; i += E) {
         const int q = a.T / nshd, rem = a.T % nshd;
-        split(dn, MTdn, i, E, i * q + min(i, rem), q + (i < rem ? 1 : 0), 1);
+        split(dn, MTdn, i, E, i * q + min(i, rem), q + (i < rem ? 1 : 0), 1, 0, pd);
     }
     if (e == 0) {
         *a.num_tiles = s_tot[0];
@@ -892,13 +901,15 @@ struct HostScan {
 };
 
 // nb near-equal blocks of `rows` rows from r0, each repeated for the mt weight tiles (weight
-// tile innermost), written from list entry `first` on
-void host_split(std::vector<int32_t>& list, int mt, int first, int ex, int r0, int rows, int nb) {
+// tile innermost); entry j = (first + i) * mt + m of its sequence goes to list position
+// j + (j >= from ? by : 0), as route_scan places them
+void host_split(std::vector<int32_t>& list, int mt, int first, int ex, int r0, int rows, int nb, int from, int by) {
     const int q = rows / nb, rem = rows % nb;
     for (int i = 0; i < nb; ++i) {
         const int n = q + (i < rem ? 1 : 0);
         for (int m = 0; m < mt; ++m) {
-            int32_t* t = &list[4 * ((size_t)(first + i) * mt + m)];
+            const int j = (first + i) * mt + m;
+            int32_t* t = &list[4 * (size_t)(j >= from ? j + by : j)];
             t[0] = ex; t[1] = r0; t[2] = n; t[3] = m;
         }
         r0 += n;
@@ -937,19 +948,21 @@ HostScan host_scan(const RouteArgs& a, const std::vector<int32_t>& blk) {
     }
     h.gu.assign(4 * (size_t)ngu * MTgu, 0);
     h.dn.assign(4 * (size_t)ndn * MTdn, 0);
+    const int shg = nsh * MTgu, shd = nshd * MTdn;
+    const int pg = shared_tiles_at(ngu * MTgu, shg, a.num_sms), pd = shared_tiles_at(ndn * MTdn, shd, a.num_sms);
     for (int i = 0; i < nsh; ++i) {
         const int q = a.T / nsh, rem = a.T % nsh;
-        host_split(h.gu, MTgu, i, E, i * q + std::min(i, rem), q + (i < rem ? 1 : 0), 1);
+        host_split(h.gu, MTgu, i, E, i * q + std::min(i, rem), q + (i < rem ? 1 : 0), 1, 0, pg);
     }
     for (int i = 0; i < nshd; ++i) {
         const int q = a.T / nshd, rem = a.T % nshd;
-        host_split(h.dn, MTdn, i, E, i * q + std::min(i, rem), q + (i < rem ? 1 : 0), 1);
+        host_split(h.dn, MTdn, i, E, i * q + std::min(i, rem), q + (i < rem ? 1 : 0), 1, 0, pd);
     }
-    int gb = nsh, db = nshd;
+    int gb = 0, db = 0;
     for (int e = 0; e < E; ++e) {
         const int run = h.counts[e], nn = (run + kGuRows - 1) / kGuRows, nd = (run + kDnRows - 1) / kDnRows;
-        if (nn > 0) host_split(h.gu, MTgu, gb, e, h.offsets[e], run, nn);
-        if (nd > 0) host_split(h.dn, MTdn, db, e, h.offsets[e], run, nd);
+        if (nn > 0) host_split(h.gu, MTgu, gb, e, h.offsets[e], run, nn, pg, shg);
+        if (nd > 0) host_split(h.dn, MTdn, db, e, h.offsets[e], run, nd, pd, shd);
         gb += nn;
         db += nd;
     }
