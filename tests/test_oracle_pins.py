@@ -230,8 +230,30 @@ def test_route_meta_invariants(T, BM):
     assert (covered == 1).all()
     assert list(tiles[:, 0]) == sorted(tiles[:, 0])
     assert m["num_tiles"] == sum((c + BM - 1) // BM for c in m["counts"])
+    # inside a group the tiles follow the rows: the first starts at the group's offset, each
+    # next one where the previous ended, and only the group's last tile may hold fewer than BM
+    for e in range(E):
+        te = tiles[tiles[:, 0] == e]
+        if m["counts"][e] == 0:
+            assert len(te) == 0
+            continue
+        assert te[0, 1] == off[e] and te[-1, 1] + te[-1, 2] == off[e + 1]
+        assert (te[1:, 1] == te[:-1, 1] + te[:-1, 2]).all()
+        assert (te[:-1, 2] == BM).all() and 1 <= te[-1, 2] <= BM
     if T == 2048:                        # the pages: 2K tokens -> 16,384 assignments, 64 per expert
         assert k * T == 16384 and m["counts"].mean() == 64.0
+
+
+def test_route_meta_short_tile_is_last_of_its_group():
+    """Hand case: expert 5 gets 3 rows, expert 9 gets 40, tile_rows 16: the block map is
+    (5, 0, 3), (9, 3, 16), (9, 19, 16), (9, 35, 8) -- the short tile closes each group."""
+    idx = np.zeros((40, 8), np.int32)
+    for t in range(40):
+        others = [e for e in range(20, 256) if e % 7 == t % 7][:6]
+        idx[t] = [9] + ([5] if t < 3 else [10 + t % 5 * 2 + 1]) + others
+    m = oracle.route_meta(idx, 256, 16)
+    te = [tuple(r) for r in m["tiles"] if r[0] in (5, 9)]
+    assert te == [(5, 0, 3), (9, 3, 16), (9, 19, 16), (9, 35, 8)]
 
 
 # ----------------------------------------------------------------------------- FFN
@@ -289,6 +311,43 @@ def test_moe_identical_experts_and_zero_shared():
     ysh = np.stack([oracle.expert_ffn(lay.shared, 0, x[t]) for t in range(4)])
     assert np.allclose(out_sh - out, ysh, rtol=1e-12, atol=1e-12)
     assert np.abs(ysh).max() > 0.01
+
+
+def _dense_swiglu(W, e, xf):
+    """SwiGLU of expert e on one row with the exact weights of _exact_weights (q / 16), numpy."""
+    g = (_unpack_codes(W.gate.codes[e]) / 16) @ xf
+    u = (_unpack_codes(W.up.codes[e]) / 16) @ xf
+    return (_unpack_codes(W.down.codes[e]) / 16) @ (g / (1 + np.exp(-g)) * u)
+
+
+def test_weighted_combine_pairs_each_weight_with_its_slot_expert():
+    """Eight distinct experts per token with exact weights and unequal routing weights: the
+    layer output is sum_j w_j SwiGLU_{e_j}(x) + SwiGLU_shared(x) (the output projection
+    weighted by the routing score, plus the shared expert: section "Reduce intermediate and
+    state traffic"), written here with numpy.  A weight paired with another slot's expert,
+    or a dropped shared term, lands far outside the tolerance (checked below)."""
+    rng = np.random.default_rng(11)
+    E, d, I, k, T = 256, 128, 64, 8, 4
+    routed = configs.ExpertWeights(_exact_weights(E, I, d, rng), _exact_weights(E, I, d, rng),
+                                   _exact_weights(E, d, I, rng))
+    shared = configs.ExpertWeights(_exact_weights(1, I, d, rng), _exact_weights(1, I, d, rng),
+                                   _exact_weights(1, d, I, rng))
+    x = gen.normal_bf16(5, 5, (T, d), std=0.05)
+    idx = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    w = np.sort(rng.uniform(0.02, 1.0, (T, k)), axis=1)[:, ::-1]
+    w = np.ascontiguousarray(w / w.sum(1, keepdims=True))
+    out = oracle.moe_tokens(x, idx, w, routed, shared)
+    for t in range(T):
+        xf = gen.bf16_bits_to_f32(x[t]).astype(np.float64)
+        ys = [_dense_swiglu(routed, e, xf) for e in idx[t]]
+        ysh = _dense_swiglu(shared, 0, xf)
+        ref = sum(w[t, j] * ys[j] for j in range(k)) + ysh
+        tol = 1e-9 * np.abs(ref).max()
+        assert np.abs(out[t] - ref).max() <= tol
+        # the pin discriminates: slots 0 and 1 swapped, or no shared expert, differ by far more
+        swapped = ref + (w[t, 1] - w[t, 0]) * (ys[0] - ys[1])
+        assert np.abs(swapped - ref).max() > 1e6 * tol
+        assert np.abs(ysh).max() > 1e6 * tol
 
 
 def test_chunking_leaves_outputs_unchanged():
