@@ -1,17 +1,25 @@
 """Benchmark of the GB300 sparse-MoE expert path (one JSON line on rank 0).
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--extras LIST|none]
+                [--impl ours|reference]
 
 A step is one pass of the whole hot path (route -> grouped FFN -> combine) over one batch of
-synthetic input of the workload.  Default workload: the 512-token prefill chunk (T=512, d=2048,
-256 experts, top-8, I=512 + shared expert), whose 455 MB of 4-bit weights exceed L2, so every
-step streams its inputs from HBM (a workload whose layer fits in L2 rotates through enough
-independent layer copies to exceed it).  Timing: W untimed steps, then K steps between CUDA events on
-the launching stream (prefill steps are replayed 8 at a time from one CUDA graph of the library
-calls; every 8th such chunk runs its steps from one graph per phase instead, with events between
-the phases that give the gate/up and down kernel times; K is rounded up to a multiple of 8),
-barrier + synchronize on both sides, max over ranks.  Multi-GPU (torchrun): every rank runs its own
-chunks (weak scaling, no collective on the data path).
+synthetic input of the workload.  Default (headline) workload: the skewed long prefill, 16,384
+tokens in four chunks of 4096 (d=2048, 256 experts, top-8, I=512 + shared expert, Zipf(1.2)
+router bias): a step is one chunk, the chunks taking turns; its 455 MB of 4-bit weights exceed
+L2, so every step streams them from HBM (a workload whose layer fits in L2 rotates through
+enough independent layer copies to exceed it).  The other workloads (the 4096- and 512-token
+chunks, the tiny layer and batch-1 decode) follow as keys of the same line under "extra", each
+with its own roofline, end-to-end number and oracle baseline (N=1 only).
+
+Timing: W warm-up steps (the first runs eagerly, the rest as the timed steps run), then exactly
+K steps between CUDA events on the launching stream, barrier + synchronize on both sides, max
+over ranks.  Prefill steps replay from CUDA graphs of the library calls, 8 steps per graph;
+every 8th block of 8 steps runs phase by phase (one graph per phase, events in between), which
+gives the per-kernel times of the roofline; a last partial block runs step by step.  Without
+--steps, K is chosen for about 1.5 s of timed work (the calibration steps count as warm-up).
+Multi-GPU (torchrun): every rank runs its own rotation of the chunks (weak scaling, no
+collective on the data path).
 
 --impl reference times the CPU oracle on bounded samples of the same workload on the host
 cores.
@@ -31,7 +39,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer routed tokens/s (prefill) & decode µs/token; % of TC/HBM roofline"
-DEFAULT_WORKLOAD = "prefill_t512_d2048"
+DEFAULT_WORKLOAD = "skew_t16384_d2048"
+EXTRA_WORKLOADS = ("prefill_t4096_d2048", "prefill_t512_d2048", "tiny_t128_d512", "decode_t1_d2048")
 
 
 def parse():
@@ -41,12 +50,17 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--extras", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated workloads reported under 'extra' (N=1 only), or 'none'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablations", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="decode: layer copies (default: the workload's); fewer for small profiling captures")
     ap.add_argument("--cpu-sample-tokens", type=int, default=32)
-    return ap.parse_args()
+    args = ap.parse_args()
+    args.ablations = not args.no_ablations
+    args.extra_list = [] if args.extras in ("", "none") else [w for w in args.extras.split(",") if w != args.workload]
+    return args
 
 
 def dist_env():
@@ -136,39 +150,71 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------- work
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the roofline kernel,
-# from an ncu full capture of the current kernels on each workload (None: not captured)
-TRAFFIC_BYTES = {
-    "prefill_t512_d2048": 322.273536e6 + 9.660928e6,     # ffn_tm_kernel<0, 0> (gate/up)
-    "prefill_t4096_d2048": 454.402304e6 + 61.936384e6,   # ffn_tm_kernel<0, 0> (gate/up)
-    "decode_t1_d2048": 17.082624e6,                       # decode_fused, one layer
-}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a workload's
+# dominant kernel, from an ncu capture of the current kernels: {workload: (kernel, bytes)}.
+# Empty until the kernels are captured again after a change (then the line reports null).
+TRAFFIC_BYTES = {}
 
 
 def algorithmic_counts(shp, counts):
-    """Per-launch algorithmic bytes and FLOPs of the gate/up and down kernels (real rows only)."""
+    """Per-launch algorithmic bytes and FLOPs of the gate/up and down kernels (real rows only):
+    the 4-bit weights of the experts that have rows (plus the shared expert), the activation
+    rows read once, h (bf16) written once and read once, the fp32 output written once."""
     T, d, I = shp.T, shp.d, shp.I
     touched = int((counts > 0).sum()) + 1                       # + the shared expert
     q4 = lambda rows, cols: rows * cols // 2 + rows * (cols // 64) * 4   # codes + bf16 scale/bias
     gu_w = touched * 2 * q4(I, d)
     dn_w = touched * q4(d, I)
     rows = 9 * T                                                # routed assignments + shared rows
-    gu_bytes = gu_w + rows * d * 2 + rows * 2 * I * 2           # weights + activation rows + h (hi|lo)
-    dn_bytes = dn_w + rows * 2 * I * 2 + T * d * 4 * 2          # weights + h + fp32 sum (read+write)
+    gu_bytes = gu_w + rows * d * 2 + rows * I * 2               # weights + activation rows + h
+    dn_bytes = dn_w + rows * I * 2 + T * d * 4                  # weights + h + fp32 weighted sum
     gu_flops = 2.0 * rows * d * 2 * I
     dn_flops = 2.0 * rows * I * d
     return dict(gu_bytes=gu_bytes, dn_bytes=dn_bytes, gu_flops=gu_flops, dn_flops=dn_flops,
                 weights_bytes=gu_w + dn_w, touched=touched)
 
 
-def run_ours(args, rank, world, local):
+def step_plan(n, multi, probe_every=None):
+    """How n consecutive steps run: blocks of `multi` steps replay one graph ("multi"); every
+    probe_every-th block runs its steps phase by phase with events in between ("probe"); a last
+    partial block runs step by step ("single").  Entries: (kind, first step)."""
+    ops, s, b = [], 0, 0
+    while s < n:
+        m = min(multi, n - s)
+        if probe_every and b % probe_every == 0:
+            ops += [("probe", s + j) for j in range(m)]
+        elif m == multi:
+            ops.append(("multi", s))
+        else:
+            ops += [("single", s + j) for j in range(m)]
+        s += m
+        b += 1
+    return ops
+
+
+def roofline_entry(kernel, P, work, ms, unit_kind, long_region, traffic):
+    """achieved = algorithmic work per launch / measured launch time; frac against the measured
+    peak (bf16: the sustained figure when the timed region is long, else the burst one)."""
+    if unit_kind == "hbm":
+        ach = work / (ms * 1e-3) / 1e9
+        return dict(bound="hbm", achieved=ach, peak=P["hbm_gbs"], unit="GB/s", frac=ach / P["hbm_gbs"],
+                    traffic=traffic, kernel=kernel, algorithmic_bytes=work, kernel_ms=ms, peak_source=P["source"])
+    ach = work / (ms * 1e-3) / 1e12
+    peak = P["bf16_tflops_sustained"] if long_region else P["bf16_tflops"]
+    return dict(bound="tensor", achieved=ach, peak=peak, unit="TFLOP/s", frac=ach / peak,
+                frac_burst=ach / P["bf16_tflops"], frac_sustained=ach / P["bf16_tflops_sustained"],
+                peak_kind="sustained" if long_region else "burst", traffic=traffic, kernel=kernel,
+                algorithmic_flops=work, kernel_ms=ms, peak_source=P["source"])
+
+
+def run_ours(wname, args, rank, world, local, headline=True):
     import torch
     import quantized_grouped_gemm_gb300 as moe
     from moe_workload import configs
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = configs.WORKLOADS[args.workload]
+    wl = configs.WORKLOADS[wname]
     sh = wl.shape
     decode = sh.T == 1
     T = wl.chunk or sh.T
@@ -183,7 +229,6 @@ def run_ours(args, rank, world, local):
     def to_dev(a):
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a)).to(dev)
 
-    # weights: `layers` independent copies (decode; small prefill layers), else one layer
     L = []
     for li in range(layers):
         lay = configs.make_layer(wl, layer=li)
@@ -194,10 +239,10 @@ def run_ours(args, rank, world, local):
         L.append(dict(wr=to_dev(lay.w_router), bias=None if lay.logit_bias is None else to_dev(lay.logit_bias),
                       pr=pr, ps=ps))
         del lay
-    # activations: prefill chunks of this rank, or decode steps
     if decode:
         nsteps_x = 1000
         x_all = to_dev(configs.make_decode_x(wl, nsteps_x))
+        xs = None
     else:
         x_full = configs.make_x(wl)
         nchunk = sh.T // T
@@ -211,127 +256,99 @@ def run_ours(args, rank, world, local):
     x_in = torch.zeros(T, sh.d, dtype=torch.int16, device=dev)
     stream = torch.cuda.Stream(device=dev)
     opts = moe.options()
+    W = max(1, args.warmup)
+    PROBE = 8
 
-    # ---- capture one step as graphs (per phase for prefill, all layers for decode)
-    n0 = moe.moe_launch_count()
-    graphs = {}
+    # ---- warm-up step 1 runs eagerly (the library's one-time set-up: kernel attributes, the
+    # one-launch decode kernel's occupancy check); then the graphs are captured
     with torch.cuda.stream(stream):
         if decode:
-            g = torch.cuda.CUDAGraph()
-            for li in range(layers):   # warm the kernels once outside capture
+            for li in range(layers):
                 moe.moe_forward(shp, x_in, L[li]["wr"], L[li]["bias"], L[li]["pr"], L[li]["ps"], rt, ws, y, opts,
                                 stream)
             stream.synchronize()
             n0 = moe.moe_launch_count()
+            g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for li in range(layers):
                     moe.moe_forward(shp, x_in, L[li]["wr"], L[li]["bias"], L[li]["pr"], L[li]["ps"], rt, ws, y, opts,
                                     stream)
-            graphs["step"] = g
+            launches_per_step = moe.moe_launch_count() - n0
+            MULTI = 1
         else:
-            # one set of phase graphs per (layer copy, resident chunk buffer): a step reads its
-            # chunk in place; step s runs layer s % layers on chunk s % chunks
+            # step s runs layer copy s % layers on resident chunk s % chunks, reading it in place
             def calls_for(lw, xc):
-                return {
-                    "route": lambda: moe.moe_route(shp, xc, lw["wr"], lw["bias"], rt, ws, opts, stream),
-                    "gate_up": lambda: moe.moe_ffn_gate_up(shp, xc, rt, lw["pr"], lw["ps"], ws, opts, stream),
-                    "down": lambda: moe.moe_ffn_down(shp, rt, lw["pr"], lw["ps"], ws, opts, stream),
-                    "combine": lambda: moe.moe_combine(shp, rt, ws, y, opts, stream),
-                }
+                return [lambda: moe.moe_route(shp, xc, lw["wr"], lw["bias"], rt, ws, opts, stream),
+                        lambda: moe.moe_ffn_gate_up(shp, xc, rt, lw["pr"], lw["ps"], ws, opts, stream),
+                        lambda: moe.moe_ffn_down(shp, rt, lw["pr"], lw["ps"], ws, opts, stream),
+                        lambda: moe.moe_combine(shp, rt, ws, y, opts, stream)]
             nsets = int(np.lcm(layers, len(xs)))
-            for gi in range(nsets):
-                for f in calls_for(L[gi % layers], xs[gi % len(xs)]).values():
-                    f()
+            for f in calls_for(L[0], xs[0]):
+                f()
             stream.synchronize()
-            # per set: the four phases as separate graphs (probe chunks, below, run these with
-            # events between them for the kernel times); and MULTI consecutive steps (a multiple
-            # of the set count) as one graph, in which consecutive kernels, also across steps,
-            # overlap their prologues through programmatic dependent launch
+            # per set: the four phases as separate graphs (probe steps run these with events in
+            # between, for the kernel times); and MULTI consecutive steps (a multiple of the set
+            # count) as one graph, in which consecutive kernels, also across steps, overlap their
+            # prologues through programmatic dependent launch
             graphs = []
             for gi in range(nsets):
-                if gi == 0:
-                    n0 = moe.moe_launch_count()
-                gc = {}
-                calls = calls_for(L[gi % layers], xs[gi % len(xs)])
-                for name, f in calls.items():
+                n0 = moe.moe_launch_count()
+                gc = []
+                for f in calls_for(L[gi % layers], xs[gi % len(xs)]):
                     g = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g, stream=stream):
                         f()
-                    gc[name] = g
+                    gc.append(g)
                 if gi == 0:
-                    launches_one_chunk = moe.moe_launch_count() - n0
+                    launches_per_step = moe.moe_launch_count() - n0
                 graphs.append(gc)
             MULTI = nsets * -(-8 // nsets)
             multi = torch.cuda.CUDAGraph()
             with torch.cuda.graph(multi, stream=stream):
                 for s in range(MULTI):
-                    for f in calls_for(L[s % layers], xs[s % len(xs)]).values():
+                    for f in calls_for(L[s % layers], xs[s % len(xs)]):
                         f()
-    launches_per_step = moe.moe_launch_count() - n0 if decode else launches_one_chunk
     torch.cuda.synchronize()
 
-    # prefill: steps run in chunks of MULTI (one graph replay; each step reads its chunk where it
-    # resides); every PROBE-th chunk runs its steps phase by phase with events in between.
-    # decode: a step copies its token's activations (4 KB) into the graph's input buffer first
-    PROBE = 8
-    if decode:
-        MULTI = 1
+    probes = []   # per probe step: [route, gate/up, down, combine] ms
 
-    def step(s, ev=None):
-        if decode:
-            x_in.copy_(x_all[s % nsteps_x:s % nsteps_x + 1], non_blocking=True)
-            graphs["step"].replay()
-        else:
-            gc = graphs[s % len(graphs)]
-            gc["route"].replay()
-            if ev is not None:
+    def run(n, with_probes):
+        for kind, s in step_plan(n, MULTI, PROBE if with_probes else None):
+            if decode:
+                x_in.copy_(x_all[s % nsteps_x:s % nsteps_x + 1], non_blocking=True)
+                g.replay()
+            elif kind == "multi":
+                multi.replay()
+            elif kind == "single":
+                for gph in graphs[s % len(graphs)]:
+                    gph.replay()
+            else:
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
                 ev[0].record(stream)
-            gc["gate_up"].replay()
-            if ev is not None:
-                ev[1].record(stream)
-            gc["down"].replay()
-            if ev is not None:
-                ev[2].record(stream)
-            gc["combine"].replay()
-
-    def chunk(c, evs=None):
-        """Steps c*MULTI .. c*MULTI + MULTI - 1."""
-        if decode:
-            step(c)
-        elif evs is None:
-            multi.replay()
-        else:
-            for j in range(MULTI):
-                step(c * MULTI + j, evs[j])
+                for i, gph in enumerate(graphs[s % len(graphs)]):
+                    gph.replay()
+                    ev[i + 1].record(stream)
+                probes.append(ev)
 
     dist = None
     if world > 1:
         import torch.distributed as dist
     with torch.cuda.stream(stream):
-        nwarm = -(-args.warmup // MULTI)
-        for c in range(nwarm):
-            chunk(c)
-        if not decode:   # the phase graphs too
-            chunk(0, [None] * MULTI)
+        run(W - 1, False)
         stream.synchronize()
-        warmup_steps = nwarm * MULTI + (0 if decode else MULTI)
-        # auto step count: about 1.5 s of timed work
-        if args.steps is None:
+        warmup_steps = W
+        if args.steps is None:       # auto: about 1.5 s of timed work (these steps count as warm-up)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            n = max(1, 24 // MULTI)
+            n = max(MULTI, 24 // MULTI * MULTI)
             e0.record(stream)
-            for c in range(n):
-                chunk(c)
+            run(n, False)
             e1.record(stream)
             e1.synchronize()
-            per = e0.elapsed_time(e1) / (n * MULTI)
+            per = e0.elapsed_time(e1) / n
+            warmup_steps += n
             K = int(min(20000, max(20, 1500.0 / max(per, 1e-3))))
         else:
-            K = args.steps
-        nchunks = -(-K // MULTI)
-        K = nchunks * MULTI
-        evs = {c: [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(MULTI)]
-               for c in range(0, nchunks, PROBE)} if not decode else {}
+            K = max(1, args.steps)
         clocks = ClockSampler(local)
         clocks.start()
         time.sleep(0.15)
@@ -341,8 +358,7 @@ def run_ours(args, rank, world, local):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for c in range(nchunks):
-            chunk(c, evs.get(c))
+        run(K, True)
         t1.record(stream)
         t1.synchronize()
         torch.cuda.synchronize()
@@ -351,22 +367,23 @@ def run_ours(args, rank, world, local):
         clk = clocks.stop()
     ms_total = max_over_ranks(t0.elapsed_time(t1), dist)
     ms_step = ms_total / K
+    long_region = ms_total > 1000.0
     rc, bits = moe.moe_read_status(ws, stream)
     assert rc == moe.MOE_OK, f"device status {rc} bits {bits}"
 
     P = peaks()
     res = dict(metric=METRIC, n_gpus=world, steps=K, warmup=warmup_steps, ms_per_step=ms_step, data="synthetic",
-               scaling="weak", vs_baseline=None, dtype="bf16", clocks=clk,
-               gpu_launches=int(launches_per_step * K))
+               scaling="weak", vs_baseline=None, dtype="bf16", clocks=clk, gpu_launches=int(launches_per_step * K))
+    traffic = TRAFFIC_BYTES.get(wl.name)
     if decode:
         us_tok_layer = ms_step * 1000.0 / layers
         res.update(value=us_tok_layer, unit="us/token/layer", higher_is_better=False)
         # router weight (bf16) + gate, up, down of 8 routed + 1 shared expert (4-bit + bf16 scale/bias per 64)
         bytes_layer = sh.E * sh.d * 2 + 9 * (3 * sh.d * sh.I // 2 + 3 * sh.d * sh.I // 64 * 4)
-        gbs = bytes_layer / (us_tok_layer * 1e-6) / 1e9
-        res["roofline"] = dict(bound="hbm", achieved=gbs, peak=P["hbm_gbs"], unit="GB/s", frac=gbs / P["hbm_gbs"],
-                               traffic=TRAFFIC_BYTES.get(wl.name), kernel="decode_fused (one launch per layer: route + gate/up + down + combine)",
-                               bytes_per_token_layer=bytes_layer, peak_source=P["source"])
+        res["roofline"] = roofline_entry("decode_fused (one launch per layer: route + gate/up + down + combine)", P,
+                                         bytes_layer, us_tok_layer * 1e-3, "hbm", long_region,
+                                         traffic[1] if traffic else None)
+        res["roofline"]["bytes_per_token_layer"] = bytes_layer
         res["config"] = dict(workload=wl.name, T=1, d=sh.d, E=sh.E, k=sh.k, I=sh.I, I_shared=sh.I_shared,
                              layers=layers, l2=f"inputs larger than L2: {layers} layer copies of the weights, "
                                                  f"{layers * layer_bytes / 1e9:.0f} GB",
@@ -374,105 +391,69 @@ def run_ours(args, rank, world, local):
     else:
         value = world * T * K / (ms_total / 1000.0)
         res.update(value=value, unit="routed tokens/s", higher_is_better=True)
-        ph = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for ce in evs.values() for e in ce])
-        gu_ms, dn_ms = float(ph[:, 0].mean()), float(ph[:, 1].mean())
+        ph = np.array([[ev[i].elapsed_time(ev[i + 1]) for i in range(4)] for ev in probes])
+        route_ms, gu_ms, dn_ms, comb_ms = (float(v) for v in ph.mean(axis=0))
         counts = rt.counts.cpu().numpy()
         A = algorithmic_counts(shp, counts)
-        # dominant kernel: gate/up. Bound: HBM when its arithmetic intensity is below the ridge
-        ai = A["gu_flops"] / A["gu_bytes"]
         ridge = P["bf16_tflops"] * 1e12 / (P["hbm_gbs"] * 1e9)
-        if ai < ridge:
-            ach = A["gu_bytes"] / (gu_ms * 1e-3) / 1e9
-            roof = dict(bound="hbm", achieved=ach, peak=P["hbm_gbs"], unit="GB/s", frac=ach / P["hbm_gbs"])
-        else:
-            ach = A["gu_flops"] / (gu_ms * 1e-3) / 1e12
-            roof = dict(bound="tensor", achieved=ach, peak=P["bf16_tflops"], unit="TFLOP/s", frac=ach / P["bf16_tflops"])
-        roof.update(traffic=TRAFFIC_BYTES.get(wl.name), kernel="ffn_tm_kernel<0> (gate/up + SwiGLU; tcgen05, dequantised weights in TMEM)", algorithmic_bytes=A["gu_bytes"],
-                    algorithmic_flops=A["gu_flops"], kernel_ms=gu_ms, peak_source=P["source"])
-        res["roofline"] = roof
+        # dominant kernel: the slower of the two FFN kernels; HBM-bound below the ridge point
+        down_dom = dn_ms > gu_ms
+        name = ("ffn_tm_kernel<1,0> (down projection + weighted sum; tcgen05, dequantised weights in TMEM)"
+                if down_dom else "ffn_tm_kernel<0,0> (gate/up + SwiGLU; tcgen05, dequantised weights in TMEM)")
+        flops, byts, kms = (A["dn_flops"], A["dn_bytes"], dn_ms) if down_dom else (A["gu_flops"], A["gu_bytes"], gu_ms)
+        hbm = flops / byts < ridge
+        tr = traffic[1] if traffic and traffic[0] == ("down" if down_dom else "gate_up") else None
+        res["roofline"] = roofline_entry(name, P, byts if hbm else flops, kms, "hbm" if hbm else "tensor",
+                                         long_region, tr)
         ffn_ms = gu_ms + dn_ms
-        res["ffn"] = dict(gate_up_ms=gu_ms, down_ms=dn_ms, ffn_tflops=(A["gu_flops"] + A["dn_flops"]) / (ffn_ms * 1e-3) / 1e12,
-                          ffn_frac_bf16_peak=(A["gu_flops"] + A["dn_flops"]) / (ffn_ms * 1e-3) / 1e12 / P["bf16_tflops"],
-                          ffn_weight_gbs=A["weights_bytes"] / (ffn_ms * 1e-3) / 1e9,
-                          experts_touched=A["touched"], other_ms=ms_step - ffn_ms)
+        ffn_tf = (A["gu_flops"] + A["dn_flops"]) / (ffn_ms * 1e-3) / 1e12
+        res["ffn"] = dict(
+            route_ms=route_ms, gate_up_ms=gu_ms, down_ms=dn_ms, combine_ms=comb_ms, probe_steps=len(probes),
+            gate_up=roofline_entry("gate/up", P, A["gu_flops"], gu_ms, "tensor", long_region, None),
+            down=roofline_entry("down", P, A["dn_flops"], dn_ms, "tensor", long_region, None),
+            gate_up_hbm=roofline_entry("gate/up", P, A["gu_bytes"], gu_ms, "hbm", long_region, None),
+            down_hbm=roofline_entry("down", P, A["dn_bytes"], dn_ms, "hbm", long_region, None),
+            ffn_tflops=ffn_tf, ffn_frac_bf16_burst=ffn_tf / P["bf16_tflops"],
+            ffn_frac_bf16_sustained=ffn_tf / P["bf16_tflops_sustained"],
+            ffn_weight_gbs=A["weights_bytes"] / (ffn_ms * 1e-3) / 1e9, experts_touched=A["touched"],
+            other_ms=ms_step - ffn_ms)
+        for key in ("gate_up", "down", "gate_up_hbm", "down_hbm"):
+            for drop in ("kernel", "traffic", "peak_source"):
+                res["ffn"][key].pop(drop, None)
         res["config"] = dict(workload=wl.name, T=T, d=sh.d, E=sh.E, k=sh.k, I=sh.I, I_shared=sh.I_shared,
                              chunks=sh.T // T, layers=layers,
                              l2=f"inputs larger than L2: {layers} layer cop{'y' if layers == 1 else 'ies'} of "
                                 f"{layer_bytes / 1e6:.0f} MB of 4-bit weights, a step reads one",
                              parallelism=f"replicas x{world}")
 
-    # ---- end to end through the public API with host buffers (pinned), copies timed
-    if not decode:
-        # Every step copies its chunk in from pinned host memory, runs moe_forward and copies its
-        # output back, all inside the timed region.  The copies run on a copy stream into two
-        # device buffers, so the input of step s+1 and the output of step s-1 move while step s
-        # computes (consecutive steps share the workspace and run in order on `stream`).
-        xh = [t.cpu().pin_memory() for t in xs[:4]]
-        cs = torch.cuda.Stream(device=dev)
-        xb = [torch.empty(T, sh.d, dtype=torch.int16, device=dev) for _ in range(2)]
-        yb = [torch.empty(T, sh.d, dtype=torch.int16, device=dev) for _ in range(2)]
-        yh = [torch.empty(T, sh.d, dtype=torch.int16).pin_memory() for _ in range(2)]
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_done = [torch.cuda.Event() for _ in range(2)]
+    res["e2e"] = e2e(moe, torch, shp, sh, T, K, L, layers, xs, rt, ws, y, x_in, stream, dev, decode,
+                     g if decode else None, world, wl)
+    if not decode and args.ablations and world == 1:
+        res["ablations"] = ablations(moe, shp, L, layers, xs, rt, ws, y, stream, T, world, wl.name)
+    del L, xs, rt, ws, y, x_in
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res, wl
 
-        def h2d(s):   # waits until step s-2 (same buffers) has finished
-            i = s & 1
-            cs.wait_event(ev_done[i])
-            with torch.cuda.stream(cs):
-                xb[i].copy_(xh[s % len(xh)], non_blocking=True)
-            ev_in[i].record(cs)
 
-        def compute(s):
-            i = s & 1
-            lw = L[s % layers]
-            stream.wait_event(ev_in[i])
-            moe.moe_forward(shp, xb[i], lw["wr"], lw["bias"], lw["pr"], lw["ps"], rt, ws, yb[i], opts, stream)
-            ev_done[i].record(stream)
-
-        def d2h(s):
-            i = s & 1
-            cs.wait_event(ev_done[i])
-            with torch.cuda.stream(cs):
-                yh[i].copy_(yb[i], non_blocking=True)
-
-        def run(n, start):
-            cs.wait_event(start)
-            h2d(0)
-            for s in range(n):
-                if s + 1 < n:
-                    h2d(s + 1)
-                compute(s)
-                d2h(s)
-
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        run(3, a)
-        torch.cuda.synchronize()
-        Ke = min(K, 2000)
-        a.record(stream)
-        run(Ke, a)
-        b.record(cs)   # after the last output copy, which follows the last step
-        b.synchronize()
-        torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b)
-        res["e2e"] = dict(value=world * T * Ke / (e_ms / 1000.0), unit="routed tokens/s",
-                          h2d_bytes_per_step=T * sh.d * 2, d2h_bytes_per_step=T * sh.d * 2,
-                          copies="pinned host buffers; copy stream overlapped with compute, two buffers")
-        if not args.no_ablations:
-            res["ablations"] = ablations(moe, shp, L, layers, xs, rt, ws, y, stream, T, world)
-    else:
+def e2e(moe, torch, shp, sh, T, K, L, layers, xs, rt, ws, y, x_in, stream, dev, decode, graph, world, wl):
+    """The same metric through the public API with host buffers: every step copies its input from
+    pinned host memory and its output back, inside the timed region."""
+    if decode:
+        from moe_workload import configs
         xh = configs.make_decode_x(wl, 16)
         xh_t = torch.from_numpy(xh.view(np.int16)).pin_memory()
         yh = torch.empty(1, sh.d, dtype=torch.int16).pin_memory()
+        layers_n = layers
         with torch.cuda.stream(stream):
             def e2e_step(s):
                 x_in.copy_(xh_t[s % 16:s % 16 + 1], non_blocking=True)
-                graphs["step"].replay()
+                graph.replay()
                 yh.copy_(y, non_blocking=True)
             for s in range(3):
                 e2e_step(s)
             stream.synchronize()
-            Ke = min(K, 200)
+            Ke = min(K, 1000)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for s in range(Ke):
@@ -480,14 +461,72 @@ def run_ours(args, rank, world, local):
             b.record(stream)
             b.synchronize()
         e_ms = a.elapsed_time(b)
-        res["e2e"] = dict(value=e_ms * 1000.0 / Ke / layers, unit="us/token/layer",
-                          h2d_bytes_per_step=sh.d * 2, d2h_bytes_per_step=sh.d * 2)
-    return res, wl
+        return dict(value=e_ms * 1000.0 / Ke / layers_n, unit="us/token/layer", h2d_bytes_per_step=sh.d * 2,
+                    d2h_bytes_per_step=sh.d * 2, steps=Ke,
+                    copies="4 KB in and out per token, in order on the compute stream (pinned host buffers)")
+    # Prefill: every step copies its chunk in from pinned host memory, runs moe_forward and copies
+    # its output back.  The copies run on a copy stream into two device buffers, so the input of
+    # step s+1 and the output of step s-1 move while step s computes (consecutive steps share the
+    # workspace and run in order on `stream`).
+    opts = moe.options()
+    xh = [t.cpu().pin_memory() for t in xs[:4]]
+    cs = torch.cuda.Stream(device=dev)
+    xb = [torch.empty(T, sh.d, dtype=torch.int16, device=dev) for _ in range(2)]
+    yb = [torch.empty(T, sh.d, dtype=torch.int16, device=dev) for _ in range(2)]
+    yh = [torch.empty(T, sh.d, dtype=torch.int16).pin_memory() for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+
+    def h2d(s):   # waits until step s-2 (same buffers) has finished
+        i = s & 1
+        cs.wait_event(ev_done[i])
+        with torch.cuda.stream(cs):
+            xb[i].copy_(xh[s % len(xh)], non_blocking=True)
+        ev_in[i].record(cs)
+
+    def compute(s):
+        i = s & 1
+        lw = L[s % layers]
+        stream.wait_event(ev_in[i])
+        moe.moe_forward(shp, xb[i], lw["wr"], lw["bias"], lw["pr"], lw["ps"], rt, ws, yb[i], opts, stream)
+        ev_done[i].record(stream)
+
+    def d2h(s):
+        i = s & 1
+        cs.wait_event(ev_done[i])
+        with torch.cuda.stream(cs):
+            yh[i].copy_(yb[i], non_blocking=True)
+
+    def run(n, start):
+        cs.wait_event(start)
+        h2d(0)
+        for s in range(n):
+            if s + 1 < n:
+                h2d(s + 1)
+            compute(s)
+            d2h(s)
+
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    run(3, a)
+    torch.cuda.synchronize()
+    Ke = min(K, 2000)
+    a.record(stream)
+    run(Ke, a)
+    b.record(cs)   # after the last output copy, which follows the last step
+    b.synchronize()
+    torch.cuda.synchronize()
+    e_ms = a.elapsed_time(b)
+    return dict(value=world * T * Ke / (e_ms / 1000.0), unit="routed tokens/s", h2d_bytes_per_step=T * sh.d * 2,
+                d2h_bytes_per_step=T * sh.d * 2, steps=Ke,
+                copies="pinned host buffers; copy stream overlapped with compute, two buffers")
 
 
-def ablations(moe, shp, L, layers, xs, rt, ws, y, stream, T, world, n=100):
+def ablations(moe, shp, L, layers, xs, rt, ws, y, stream, T, world, wname, n=50):
     """Outside the timed region: the step launched eagerly through moe_forward with the default
-    design and with each ablation of it: the host round trip of the routing counts
+    design and with variants of it -- the largest token block of the grouped GEMMs
+    (moe_options.gemm_rows, the pages' tile-size choice), and for the 512-token chunk the two
+    mechanisms the pages measure: the host round trip of the routing counts
     (moe_options.host_routing, one stream synchronisation per step) and dequantisation as a
     separate pass that writes bf16 weights before the GEMMs (moe_options.unfused_dequant)."""
     import torch
@@ -510,22 +549,29 @@ def ablations(moe, shp, L, layers, xs, rt, ws, y, stream, T, world, n=100):
         assert rc == moe.MOE_OK, f"device status {rc} bits {bits}"
         return a.elapsed_time(b) / n
 
-    dev_ms = eager(moe.options(), ws)
-    host_ms = eager(moe.options(host_routing=1), ws)
-    uf = moe.options(unfused_dequant=1)
-    ws_u = moe.workspace(shp, uf)
-    uf_ms = eager(uf, ws_u)
-    del ws_u
     tok_s = lambda ms: world * T / (ms / 1000.0)
-    return dict(
-        launch=f"eager moe_forward, {n} steps each (no CUDA graph)",
-        default=dict(ms_per_step=dev_ms, value=tok_s(dev_ms)),
-        host_routing=dict(what="counts to the host, scan and block map there, results back, then scatter "
-                               "(one stream sync per step)",
-                          ms_per_step=host_ms, value=tok_s(host_ms), slowdown=host_ms / dev_ms),
-        unfused_dequant=dict(what="every expert's weights of a projection dequantised to bf16 in HBM by a separate "
-                                  "kernel, then streamed by the same grouped GEMM",
-                             ms_per_step=uf_ms, value=tok_s(uf_ms), slowdown=uf_ms / dev_ms))
+    dev_ms = eager(moe.options(), ws)
+    out = dict(launch=f"eager moe_forward, {n} steps each (no CUDA graph)",
+               default=dict(ms_per_step=dev_ms, value=tok_s(dev_ms)))
+    rows = {}
+    for r in (16, 32, 64, 128):
+        ms = eager(moe.options(gemm_rows=r), ws)
+        rows[str(r)] = dict(ms_per_step=ms, value=tok_s(ms), vs_default=ms / dev_ms)
+    out["gemm_rows"] = dict(what="largest token block of the grouped GEMMs (moe_options.gemm_rows; default 128)",
+                            **rows)
+    if wname == "prefill_t512_d2048":
+        host_ms = eager(moe.options(host_routing=1), ws)
+        uf = moe.options(unfused_dequant=1)
+        ws_u = moe.workspace(shp, uf)
+        uf_ms = eager(uf, ws_u)
+        del ws_u
+        out["host_routing"] = dict(what="counts to the host, scan and block map there, results back, then scatter "
+                                        "(one stream sync per step)",
+                                   ms_per_step=host_ms, value=tok_s(host_ms), slowdown=host_ms / dev_ms)
+        out["unfused_dequant"] = dict(what="every expert's weights of a projection dequantised to bf16 in HBM by a "
+                                           "separate kernel, then streamed by the same grouped GEMM",
+                                      ms_per_step=uf_ms, value=tok_s(uf_ms), slowdown=uf_ms / dev_ms)
+    return out
 
 
 # ------------------------------------------------------------------------------------- oracle
@@ -603,10 +649,21 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("gloo")
-    res, wl = run_ours(args, rank, world, local)
-    if rank == 0:
+    res, wl = run_ours(args.workload, args, rank, world, local)
+    if rank == 0 and world == 1:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_tokens if wl.shape.T != 1 else 16)
+        extra = {}
+        for name in args.extra_list:
+            r, w2 = run_ours(name, args, rank, world, local, headline=False)
+            if not args.no_cpu_baseline:
+                r["cpu_baseline"] = cpu_baseline(w2, args.cpu_sample_tokens if w2.shape.T != 1 else 16)
+            for key in ("metric", "n_gpus", "data", "scaling", "vs_baseline", "dtype"):
+                r.pop(key, None)
+            extra[name] = r
+        if extra:
+            res["extra"] = extra
+    if rank == 0:
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist

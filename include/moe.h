@@ -32,7 +32,12 @@
  *     range, a bounded wait that ran out) set bits of the status word kept in the workspace;
  *     read it with moe_read_status (a synchronising debug call).
  *   - Supported shapes: E = 256, k = 8, group = 64, d % 256 == 0, I % 128 == 0,
- *     I_shared == I, d % 128 == 0, 0 <= T <= 65536.  T = 0 is a no-op.
+ *     I_shared == I, 0 <= T <= 65536, d <= 7168, I <= 8192.  T = 0 is a no-op.
+ *     I % 128 (not only a whole number of 64-weight groups) is a deliberate restriction:
+ *     every gate/up weight tile is one 128-row tensor-core operand (M = 128, one TMEM lane
+ *     per row) and the packed layout cuts rows in 128s; an I with a 64-row remainder would
+ *     need zero-padded rows in the packed weights and masked writes of h.  Other shapes
+ *     return MOE_ERR_UNSUPPORTED.
  */
 #ifndef MOE_H
 #define MOE_H
@@ -132,7 +137,16 @@ typedef struct moe_options {
                                grows accordingly, see moe_workspace_bytes) and the GEMM then
                                streams those.  Same bf16 weights, same results bit for bit.
                                Ignored by the decode path. */
-    int reserved[2];
+    int gemm_rows;          /* prefill: largest number of token rows in one grouped-GEMM block, 16, 32,
+                               64 or 128 (default 128; 0 takes the default, other values are an
+                               argument error).  Each expert's rows are cut into near-equal blocks
+                               of at most this many rows, and every block streams its expert's
+                               weights once per projection ("Match tile size to expert load" on the
+                               page).  Used by moe_route, which writes the GEMM tile lists that
+                               moe_grouped_ffn reads.  Every value gives the same routing and the
+                               same outputs up to fp32 summation order.  Ignored by the decode
+                               path. */
+    int reserved[1];
 } moe_options;
 
 /* Human-readable text for a return code. */
@@ -214,9 +228,11 @@ int moe_combine(const moe_shape* shape, const moe_routing* routing, void* worksp
 
 /* The whole layer: moe_route, moe_grouped_ffn, moe_combine in one call.
  * One token (T = 1, decode): with options.decode_path = MOE_DECODE_AUTO the layer is one
- * kernel launch (routing, both projections and the combine) when I % 256 == 0 and all of its
- * (k+1) * I/256 clusters of 8 CTAs fit on the GPU at once; otherwise the three decode kernels
- * run.  Decode kernels are launched with programmatic dependent launch: they read
+ * kernel launch (routing, both projections and the combine) when it has at most 72 units of
+ * work -- a unit is one 128-row slice of h of one of the k+1 experts, so (k+1) * I/128 <= 72,
+ * i.e. I <= 1024 -- and all of its (k+1) * I/128 clusters of 4 CTAs (256 threads each) are
+ * resident on the GPU at once (cudaOccupancyMaxActiveClusters, checked once per shape);
+ * otherwise the three decode kernels run.  Decode kernels are launched with programmatic dependent launch: they read
  * w_router_dev, logit_bias_dev and the packed weights before the previous kernel on the
  * stream has finished (x_dev and the workspace only after), so those inputs must not be
  * written by the kernel launched just before this call on the same stream (moe_pack_weights
@@ -249,9 +265,10 @@ unsigned long long moe_launch_count(void);
  * MOE_STATIC_SCRATCH_BYTES in the library's device memory, which every GPU that loads the
  * library holds until the process exits.
  * - Shapes whose scratch (256 + d*4 + 8*E*4 + 18*I*4 + 64*E bytes, each part rounded up to
- *   256) exceeds the array are rejected with MOE_ERR_WORKSPACE, before any CUDA call;
- *   T != 1 gives MOE_ERR_UNSUPPORTED.  Other checks as moe_forward; the one-launch kernel
- *   runs when moe_forward would run it.
+ *   256) exceeds the array are rejected with MOE_ERR_WORKSPACE; T != 1 gives
+ *   MOE_ERR_UNSUPPORTED.  Both are checked before any pointer argument and before any CUDA
+ *   call.  Other checks as moe_forward; the one-launch kernel runs when moe_forward would run
+ *   it, else the three decode kernels (e.g. I = 1152, whose 81 units do not fit at once).
  * - No cudaMalloc/cudaFree or allocating library call is made.  The first call on a device
  *   looks up the array's device address (cudaGetSymbolAddress); make that first call before
  *   any stream capture.

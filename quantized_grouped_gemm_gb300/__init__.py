@@ -49,14 +49,17 @@ DECODE_AUTO, DECODE_GEMV = 0, 1
 
 
 def options(tile_rows: int = 32, decode_max_tokens: int = 1, decode_path: int = DECODE_AUTO,
-            deterministic: int = 0, host_routing: int = 0, unfused_dequant: int = 0) -> _lib.moe_options:
+            deterministic: int = 0, host_routing: int = 0, unfused_dequant: int = 0,
+            gemm_rows: int = 0) -> _lib.moe_options:
     """decode_path: DECODE_AUTO (one fused launch per token when it fits) or DECODE_GEMV.
     deterministic: 1 = prefill sums each token's rows in a fixed order at every size.
     host_routing: 1 = ablation of GPU-resident routing: the scan and block map run on the
     host after a device-to-host copy of the counts (synchronises the stream; same results).
     unfused_dequant: 1 = ablation of on-chip dequantisation: each FFN call first writes the
-    projection's weights as bf16 into the (larger) workspace, then streams them (same results)."""
-    return _lib.moe_options(tile_rows, decode_max_tokens, decode_path, deterministic, host_routing, unfused_dequant)
+    projection's weights as bf16 into the (larger) workspace, then streams them (same results).
+    gemm_rows: 16, 32, 64 or 128 = largest token block of the grouped GEMMs (0: default 128)."""
+    return _lib.moe_options(tile_rows, decode_max_tokens, decode_path, deterministic, host_routing, unfused_dequant,
+                            gemm_rows)
 
 
 def _p(t: Optional[torch.Tensor]):

@@ -45,7 +45,7 @@ class moe_routing(ctypes.Structure):
 class moe_options(ctypes.Structure):
     _fields_ = [("tile_rows", ctypes.c_int), ("decode_max_tokens", ctypes.c_int), ("decode_path", ctypes.c_int),
                 ("deterministic", ctypes.c_int), ("host_routing", ctypes.c_int),
-                ("unfused_dequant", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
+                ("unfused_dequant", ctypes.c_int), ("gemm_rows", ctypes.c_int), ("reserved", ctypes.c_int * 1)]
 
 
 _SPS = ctypes.POINTER(moe_shape)

@@ -68,6 +68,7 @@ struct Opts {
     bool deterministic = false;
     bool host_routing = false;
     bool unfused_dequant = false;
+    int gemm_rows = kGemmRowsDefault;
 };
 
 static int get_opts(const moe_options* o, Opts* out) {
@@ -85,6 +86,8 @@ static int get_opts(const moe_options* o, Opts* out) {
         r.host_routing = o->host_routing == 1;
         if (o->unfused_dequant != 0 && o->unfused_dequant != 1) return MOE_ERR_INVALID_ARG;
         r.unfused_dequant = o->unfused_dequant == 1;
+        if (o->gemm_rows != 0 && !gemm_rows_valid(o->gemm_rows)) return MOE_ERR_INVALID_ARG;
+        if (o->gemm_rows != 0) r.gemm_rows = o->gemm_rows;
     }
     *out = r;
     return MOE_OK;
@@ -115,6 +118,7 @@ static RouteArgs route_args(const moe_shape* s, const uint16_t* x, const uint16_
                             const moe_routing* rt, void* ws, const Opts& o) {
     RouteArgs a{};
     a.T = s->T; a.d = s->d; a.E = s->E; a.k = s->k; a.I = s->I; a.tile_rows = o.tile_rows;
+    a.gu_rows = o.gemm_rows; a.dn_rows = o.gemm_rows;
     a.x = x; a.w_router = wr; a.bias = bias;
     a.topk_idx = rt->topk_idx_dev; a.topk_w = rt->topk_w_dev; a.counts = rt->counts_dev;
     a.offsets = rt->offsets_dev; a.perm = rt->perm_dev; a.pos = rt->pos_dev; a.tiles = rt->tiles_dev;

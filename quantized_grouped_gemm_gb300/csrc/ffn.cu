@@ -315,6 +315,11 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                     }
                     // (the wait above also means that the ready barrier's phase for K block
                     // it - 8 has completed: its MMAs were issued)
+#ifdef MOE_TEST_DROP_TOKEN_BLOCK
+                    // timeout test build only: CTA 0 never arms this K block's ready barrier, so
+                    // the MMA threads' bounded wait on it runs out and the CTA unwinds
+                    if (blockIdx.x == 0 && it == (uint32_t)(MOE_TEST_DROP_TOKEN_BLOCK)) continue;
+#endif
                     uint64_t* rdy = &b->ready[it % kTmKD];
                     mbar_arrive_expect_tx(rdy, C::PARTS * N * 128);
                     uint8_t* dst = xring + xs * C::XS;
@@ -477,11 +482,14 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             }
             if (!kDown) {
                 const DSlots ds = d_slots(sc, N, false);
+                bool failed = false;
                 if (et == 0 && (!mbar_wait(&b->d_full[ds.s0], use[ds.s0] & 1, abort) ||
-                                (ds.two && !mbar_wait(&b->d_full[ds.s1], use[ds.s1] & 1, abort))))
+                                (ds.two && !mbar_wait(&b->d_full[ds.s1], use[ds.s1] & 1, abort)))) {
                     tm_abort(abort, p.status);
-                named_bar_sync(2, kTmEpiThreads);
-                if (*abort) { ok = false; break; }
+                    failed = true;
+                }
+                // one decision for all epilogue warps (see named_bar_or)
+                if (named_bar_or(2, kTmEpiThreads, failed || *abort != 0)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t td0 = tlane + ds.col0, td1 = tlane + ds.col1;   // this lane quadrant's D_0, D_1
                 if (et == 0) TM_TRACE(TT_ET, tcount);
@@ -537,9 +545,13 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                 for (int m = 0; m < 2; ++m) {
                     const uint32_t dj = 2 * tcount + m;   // use j of the slot ring: slot j % 3, phase j / 3
                     const int dsl = (int)(dj % 3);
-                    if (et == 0 && !mbar_wait(&b->d_full[dsl], (dj / 3) & 1, abort)) tm_abort(abort, p.status);
-                    named_bar_sync(2, kTmEpiThreads);   // (also: the weight / token tables are written)
-                    if (*abort) { ok = false; break; }
+                    bool failed = false;
+                    if (et == 0 && !mbar_wait(&b->d_full[dsl], (dj / 3) & 1, abort)) {
+                        tm_abort(abort, p.status);
+                        failed = true;
+                    }
+                    // (also: the weight / token tables are written); one decision for all warps
+                    if (named_bar_or(2, kTmEpiThreads, failed || *abort != 0)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t td = tlane + C::DCOL0 + 128u * dsl;
                     for (int c0 = 0; c0 < N; c0 += 32, ++chunk) {

@@ -74,18 +74,15 @@ struct WsLayout {
 
 constexpr int kRouteBlockTokens = 32;   // tokens per routing block (one warp, one bitmask)
 constexpr int kMaxN = 128;              // max token rows of a GEMM tile (MMA M)
-#ifndef MOE_GU_ROWS
-#define MOE_GU_ROWS 128                 // token rows of a gate/up block (TMEM-operand FFN)
-#endif
-#ifndef MOE_DN_ROWS
-#define MOE_DN_ROWS 128                 // token rows of a down-projection block (TMEM-operand FFN)
-#endif
 constexpr int kDecodeMaxT = 8;          // largest T the decode (GEMV) kernels take
-// token rows of a gate/up and of a down-projection block (smaller blocks were measured slower
-// at 4096 tokens: per-token dequant and MMA issue outweigh the overlap they allow)
-constexpr int kGuRows = MOE_GU_ROWS;
-constexpr int kDnRows = MOE_DN_ROWS;
-static_assert(kGuRows % 16 == 0 && kGuRows <= kMaxN && kDnRows % 16 == 0 && kDnRows <= kMaxN, "block rows");
+// Token rows of a GEMM block (moe_options.gemm_rows; one value for gate/up and down): an expert's
+// rows are cut into near-equal blocks of at most this many rows.  128 by default: smaller blocks
+// were measured slower at 4096 tokens (per-token dequant and MMA issue outweigh the overlap they
+// allow, and every block re-reads its expert's weights).  The workspace's tile lists are sized
+// for the smallest block.
+constexpr int kGemmRowsDefault = 128;
+constexpr int kGemmRowsMin = 16;
+inline bool gemm_rows_valid(int r) { return r == 16 || r == 32 || r == 64 || r == 128; }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -109,11 +106,6 @@ inline int router_kslices(int T, int d) {
     return ks;
 }
 
-inline int gemm_ntile_bound(int rows_total, int groups) {
-    // tiles of <= kMaxN rows, near-equal split per group: at most rows/kMaxN + groups
-    return rows_total / kMaxN + groups + 1;
-}
-
 // Decode scratch of the GEMV kernels: router logits fp32 [8][E], g/u sums fp32 [8][k+1][2][I].
 inline size_t decode_scratch_bytes(int d, int E, int k, int I) {
     (void)d;
@@ -124,13 +116,12 @@ inline WsLayout ws_layout(const moe_shape& s) {
     WsLayout L{};
     const int T = s.T, d = s.d, E = s.E, k = s.k, I = s.I;
     L.nblk = (T + kRouteBlockTokens - 1) / kRouteBlockTokens;
-    const int shared_nt = (T + kGuRows - 1) / kGuRows;
-    const int routed_nt = k * T / kGuRows + E + 1;
+    // GEMM blocks of at most kGemmRowsMin rows (the smallest option): at most
+    // rows / kGemmRowsMin + groups per expert set, times the weight tiles
+    const int shared_nt = (T + kGemmRowsMin - 1) / kGemmRowsMin;
+    const int routed_nt = k * T / kGemmRowsMin + E + 1;
     L.max_gu = (routed_nt + shared_nt) * (I / kTileRows);
-    // down blocks of at most kDnRows rows: at most rows/kDnRows + groups per expert set
-    const int shared_nd = (T + kDnRows - 1) / kDnRows;
-    const int routed_nd = k * T / kDnRows + E + 1;
-    L.max_dn = (routed_nd + shared_nd) * (d / 256);
+    L.max_dn = (routed_nt + shared_nt) * (d / 256);
     size_t o = 0;
     L.status = o; o = align_up(o + 64 * 4, 256);
     L.rpart = o; o = align_up(o + (size_t)router_kslices(T, d) * T * E * 4, 256);
@@ -173,8 +164,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // A wait gives up after this many SM cycles (about 2 s at 2 GHz); the kernel then records
-// MOE_STATUS_TIMEOUT and unwinds.  clock64 is cheap to read, unlike %globaltimer.
-constexpr long long kWaitLimitCycles = 4000000000ll;
+// MOE_STATUS_TIMEOUT and unwinds.  clock64 is cheap to read, unlike %globaltimer.  (The
+// timeout test builds a separate copy of the library with a shorter limit.)
+#ifndef MOE_WAIT_LIMIT_CYCLES
+#define MOE_WAIT_LIMIT_CYCLES 4000000000ll
+#endif
+constexpr long long kWaitLimitCycles = MOE_WAIT_LIMIT_CYCLES;
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -286,6 +281,24 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 // Hardware named barrier (ids 1..15; 0 is __syncthreads): waiting warps use no issue slots.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also ORs a predicate over its threads: all of them get the same answer,
+// so a decision taken right after it (such as unwinding) is the same in every warp that waits
+// on the barrier.  (Reading a shared flag after a plain barrier is not: another role may set it
+// between two warps' reads, and the warps that go on would then wait at the next barrier for
+// the ones that left.)
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -603,6 +616,7 @@ __device__ __forceinline__ void prefetch_l2_range(const uint8_t* p, size_t bytes
 // ------------------------------------------------------------------------------------
 struct RouteArgs {
     int T, d, E, k, tile_rows;
+    int gu_rows, dn_rows;      // token rows of a gate/up and of a down GEMM block (at most)
     const uint16_t* x;
     const uint16_t* w_router;
     const float* bias;

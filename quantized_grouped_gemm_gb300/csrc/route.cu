@@ -573,17 +573,17 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     }
     if (e == E - 1) s_tot[0] = tbase + nt;
 
-    // GEMM tile lists: an expert's rows split into near-equal token blocks (gate/up: at most
-    // kGuRows rows; down: at most kDnRows); each block is repeated for every weight tile (weight
-    // tile innermost, so the CTAs that run at the same time share the block's activation rows
+    // GEMM tile lists: an expert's rows split into near-equal token blocks of at most
+    // a.gu_rows (gate/up) and a.dn_rows (down) rows (moe_options.gemm_rows); each block is
+    // repeated for every weight tile (weight tile innermost, so the CTAs that run at the same time share the block's activation rows
     // in L2).  The shared expert (expert index E) covers token rows 0..T-1 in full blocks; its
     // tiles are inserted where the CTAs run one tile fewer (shared_tiles_at), the experts'
     // tiles follow in expert order around them.
     const int MTgu = a.I / kTileRows, MTdn = a.d / 256;   // 128 gate+up row pairs; 256-row down tiles
-    const int nn = (run + kGuRows - 1) / kGuRows;
-    const int nd = (run + kDnRows - 1) / kDnRows;
-    const int nsh = (a.T + kGuRows - 1) / kGuRows;
-    const int nshd = (a.T + kDnRows - 1) / kDnRows;
+    const int nn = (run + a.gu_rows - 1) / a.gu_rows;
+    const int nd = (run + a.dn_rows - 1) / a.dn_rows;
+    const int nsh = (a.T + a.gu_rows - 1) / a.gu_rows;
+    const int nshd = (a.T + a.dn_rows - 1) / a.dn_rows;
     const int nbase = block_exclusive_scan256(nn, s_tmp);
     if (e == E - 1) s_tot[1] = nbase + nn;
     named_bar_sync(1, 256);
@@ -940,11 +940,11 @@ HostScan host_scan(const RouteArgs& a, const std::vector<int32_t>& blk) {
         }
     h.num_tiles = (int32_t)(h.tiles.size() / 3);
     const int MTgu = a.I / kTileRows, MTdn = a.d / 256;
-    const int nsh = (a.T + kGuRows - 1) / kGuRows, nshd = (a.T + kDnRows - 1) / kDnRows;
+    const int nsh = (a.T + a.gu_rows - 1) / a.gu_rows, nshd = (a.T + a.dn_rows - 1) / a.dn_rows;
     int ngu = nsh, ndn = nshd;
     for (int e = 0; e < E; ++e) {
-        ngu += (h.counts[e] + kGuRows - 1) / kGuRows;
-        ndn += (h.counts[e] + kDnRows - 1) / kDnRows;
+        ngu += (h.counts[e] + a.gu_rows - 1) / a.gu_rows;
+        ndn += (h.counts[e] + a.dn_rows - 1) / a.dn_rows;
     }
     h.gu.assign(4 * (size_t)ngu * MTgu, 0);
     h.dn.assign(4 * (size_t)ndn * MTdn, 0);
@@ -960,7 +960,7 @@ HostScan host_scan(const RouteArgs& a, const std::vector<int32_t>& blk) {
     }
     int gb = 0, db = 0;
     for (int e = 0; e < E; ++e) {
-        const int run = h.counts[e], nn = (run + kGuRows - 1) / kGuRows, nd = (run + kDnRows - 1) / kDnRows;
+        const int run = h.counts[e], nn = (run + a.gu_rows - 1) / a.gu_rows, nd = (run + a.dn_rows - 1) / a.dn_rows;
         if (nn > 0) host_split(h.gu, MTgu, gb, e, h.offsets[e], run, nn, pg, shg);
         if (nd > 0) host_split(h.dn, MTdn, db, e, h.offsets[e], run, nd, pd, shd);
         gb += nn;

@@ -40,9 +40,9 @@ uint8_t* scratch_address(int dev) {
     return g_scratch_ptr[dev];
 }
 
-// Scratch layout inside the array: status + counters, fp32 sum [d], logits [8][E] followed by
-// g/u [k+1][2][I] (GEMV kernels) or the per-unit partial outputs (fused kernel), then the
-// fused kernel's tagged logits.
+// Scratch layout inside the array: status word and counters, the fp32 output sum [d] (both
+// decode paths add into it), the GEMV path's router logits [8][E] and g/u sums [k+1][2][I],
+// then the fused kernel's eight copies of the tagged logits [8][E].
 WsLayout static_layout(const moe_shape& s) {
     WsLayout L{};
     size_t o = 0;
@@ -66,9 +66,13 @@ extern "C" int moe_forward_decode_static(const moe_shape* s, const uint16_t* x, 
                                          const float* logit_bias, const void* packed_routed,
                                          const void* packed_shared, const moe_routing* rt, uint16_t* y,
                                          void* stream) {
+    // the shape and its scratch size first: a shape that cannot run is refused whatever the
+    // pointers are
     int rc = moe_check_shape(s);
     if (rc != MOE_OK) return rc;
     if (s->T != 1) return MOE_ERR_UNSUPPORTED;
+    const WsLayout L = static_layout(*s);
+    if (L.total > (size_t)MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
     if (!rt || !rt->topk_idx_dev || !rt->topk_w_dev || !rt->counts_dev || !rt->offsets_dev || !rt->perm_dev ||
         !rt->pos_dev || !rt->tiles_dev || !rt->num_tiles_dev)
         return MOE_ERR_INVALID_ARG;
@@ -76,8 +80,6 @@ extern "C" int moe_forward_decode_static(const moe_shape* s, const uint16_t* x, 
         !aligned16(y) || (reinterpret_cast<uintptr_t>(packed_routed) & 255) ||
         (reinterpret_cast<uintptr_t>(packed_shared) & 255) || (logit_bias && (reinterpret_cast<uintptr_t>(logit_bias) & 3)))
         return MOE_ERR_INVALID_ARG;
-    const WsLayout L = static_layout(*s);
-    if (L.total > (size_t)MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
     uint8_t* ws = scratch_address(dev);
@@ -111,6 +113,7 @@ extern "C" int moe_forward_decode_static(const moe_shape* s, const uint16_t* x, 
 
     RouteArgs ra{};
     ra.T = 1; ra.d = s->d; ra.E = s->E; ra.k = s->k; ra.I = s->I; ra.tile_rows = 32;
+    ra.gu_rows = ra.dn_rows = kGemmRowsDefault;
     ra.x = x; ra.w_router = w_router; ra.bias = logit_bias;
     ra.topk_idx = rt->topk_idx_dev; ra.topk_w = rt->topk_w_dev; ra.counts = rt->counts_dev;
     ra.offsets = rt->offsets_dev; ra.perm = rt->perm_dev; ra.pos = rt->pos_dev; ra.tiles = rt->tiles_dev;

@@ -43,6 +43,11 @@ def test_shape_checks(lib):
     for bad, rc in [((512, 2048, 128, 8, 512, 512, 64), _lib.MOE_ERR_UNSUPPORTED),
                     ((512, 2000, 256, 8, 512, 512, 64), _lib.MOE_ERR_UNSUPPORTED),
                     ((512, 2048, 256, 8, 500, 500, 64), _lib.MOE_ERR_UNSUPPORTED),
+                    ((512, 2048, 256, 8, 192, 192, 64), _lib.MOE_ERR_UNSUPPORTED),   # I % 128 != 0
+                    ((512, 2048, 256, 8, 640, 640, 64), _lib.MOE_OK),
+                    ((512, 7168 + 256, 256, 8, 512, 512, 64), _lib.MOE_ERR_UNSUPPORTED),
+                    ((512, 2048, 256, 8, 8192 + 128, 8192 + 128, 64), _lib.MOE_ERR_UNSUPPORTED),
+                    ((65537, 2048, 256, 8, 512, 512, 64), _lib.MOE_ERR_UNSUPPORTED),
                     ((512, 2048, 256, 8, 512, 256, 64), _lib.MOE_ERR_UNSUPPORTED),
                     ((512, 2048, 256, 8, 512, 512, 32), _lib.MOE_ERR_UNSUPPORTED),
                     ((-1, 2048, 256, 8, 512, 512, 64), _lib.MOE_ERR_INVALID_ARG)]:
@@ -95,18 +100,20 @@ def _static_scratch_needed(d, I, E=256, k=8):
 
 
 def test_static_scratch_rejects_what_does_not_fit(lib):
-    """Rejected on the host before any CUDA call (the pointers are never dereferenced)."""
+    """The shape and its scratch size are checked before any pointer, so null pointers
+    everywhere still give the size error (nothing is launched, no GPU needed)."""
     big = _lib.moe_shape(1, 7168, 256, 8, 8192, 8192, 64)
-    # guard: only call with dummy pointers when the shape is certain to be refused
     assert _static_scratch_needed(7168, 8192) > _static_scratch_limit()
     assert _static_scratch_needed(2048, 512) <= _static_scratch_limit()   # the decode workload fits
-    rt = _lib.moe_routing(*([256] * 8))
-    fake = ctypes.c_void_p(1 << 20)   # 256-byte aligned, never used
-    rc = lib.moe_forward_decode_static(ctypes.byref(big), fake, fake, None, fake, fake, ctypes.byref(rt), fake, None)
+    rc = lib.moe_forward_decode_static(ctypes.byref(big), None, None, None, None, None, None, None, None)
     assert rc == _lib.MOE_ERR_WORKSPACE
     two = _lib.moe_shape(2, 1024, 256, 8, 256, 256, 64)
-    rc = lib.moe_forward_decode_static(ctypes.byref(two), fake, fake, None, fake, fake, ctypes.byref(rt), fake, None)
+    rc = lib.moe_forward_decode_static(ctypes.byref(two), None, None, None, None, None, None, None, None)
     assert rc == _lib.MOE_ERR_UNSUPPORTED
+    # a shape that fits gets to the pointer checks: null pointers are an argument error
+    fits = _lib.moe_shape(1, 2048, 256, 8, 512, 512, 64)
+    rc = lib.moe_forward_decode_static(ctypes.byref(fits), None, None, None, None, None, None, None, None)
+    assert rc == _lib.MOE_ERR_INVALID_ARG
 
 
 def test_host_routing_option_is_validated(lib):
@@ -140,3 +147,15 @@ def test_deterministic_option_is_validated(lib):
         o = _lib.moe_options(32, 1, 0, v)
         n = lib.moe_workspace_bytes(ctypes.byref(s), ctypes.byref(o))
         assert (n > 0) == ok, (v, n)
+
+
+def test_gemm_rows_option_is_validated(lib):
+    """moe_options.gemm_rows takes 0 (default 128) or 16, 32, 64, 128; anything else is an
+    argument error.  The workspace does not depend on it (its tile lists are sized for 16)."""
+    s = _lib.moe_shape(4096, 2048, 256, 8, 512, 512, 64)
+    base = lib.moe_workspace_bytes(ctypes.byref(s), None)
+    for v, ok in ((0, True), (16, True), (32, True), (64, True), (128, True), (48, False), (256, False),
+                  (-16, False)):
+        o = _lib.moe_options(32, 1, 0, 0, 0, 0, v)
+        n = lib.moe_workspace_bytes(ctypes.byref(s), ctypes.byref(o))
+        assert (n == base) if ok else (n == 0), (v, n)

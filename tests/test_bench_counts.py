@@ -35,7 +35,10 @@ def test_prefill_counts_closed_form():
     assert per_matrix == 589824
     assert A["touched"] == 257                                       # every expert + the shared one
     rows = 9 * T                                                     # 8 routed rows per token + shared
-    assert A["gu_bytes"] == 257 * 2 * per_matrix + rows * d * 2 + rows * 2 * I * 2 == 331481088
+    # weights + the activation rows read once + h (bf16) written once
+    assert A["gu_bytes"] == 257 * 2 * per_matrix + rows * d * 2 + rows * I * 2 == 326762496
+    # weights + h read once + the fp32 weighted sum written once
+    assert A["dn_bytes"] == 257 * per_matrix + rows * I * 2 + T * d * 4 == 160497664
     assert A["gu_flops"] == 2.0 * rows * d * 2 * I == 19327352832.0
     assert A["dn_flops"] == A["gu_flops"] / 2
     assert A["weights_bytes"] == 257 * 3 * per_matrix
@@ -56,3 +59,17 @@ def test_weight_bytes_agree_with_the_packed_size(lib):
         counts = np.zeros(256, dtype=np.int64)
         A = bench.algorithmic_counts(_Shape(64, d, I), counts)      # touched = the shared expert only
         assert A["weights_bytes"] == packed - 256, (d, I)
+
+
+@pytest.mark.parametrize("n,multi,probe", [(20, 8, 8), (5, 8, 8), (8, 8, None), (100, 8, 8), (7, 4, None), (1, 1, 8)])
+def test_step_plan_runs_exactly_n_steps(n, multi, probe):
+    """bench.py times exactly the requested steps: graph blocks of `multi` steps, probe blocks
+    (phase by phase) every `probe` blocks starting with the first, and a partial block last."""
+    plan = bench.step_plan(n, multi, probe)
+    steps = []
+    for kind, s in plan:
+        steps += list(range(s, s + multi)) if kind == "multi" else [s]
+    assert steps == list(range(n))
+    if probe:
+        assert plan[0][0] == "probe"
+    assert all(s % multi == 0 for kind, s in plan if kind == "multi")

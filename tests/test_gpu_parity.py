@@ -46,29 +46,6 @@ def test_small_full_parity(wl, split):
     assert_output_close(y_to_f64(y)[: shp.T], out_ref, wl.name)
 
 
-FULL = ["prefill_t512_d2048", "prefill_t4096_d2048", "skew_t16384_d2048"]
-
-
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_routing_and_sampled_outputs(name):
-    wl = configs.WORKLOADS[name]
-    x_all = configs.make_x(wl)
-    T = wl.chunk or wl.shape.T
-    shp, lay, _, dl = _setup(wl, x_rows=x_all[:T])
-    chunks = range(0, wl.shape.T, T)
-    for ci, c0 in enumerate(chunks):
-        if ci > 1:       # skewed case: chunks 0 and 1 of 4 (each 4096 tokens)
-            break
-        x = np.ascontiguousarray(x_all[c0:c0 + T])
-        rt, ws, y = run_forward(shp, dl, to_dev(x))
-        ref = oracle.route(x, lay.w_router, lay.logit_bias)
-        assert_routing_equal(routing_to_host(rt, T), ref)
-        rng = np.random.default_rng(ci)
-        toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 14, replace=False)])).astype(np.int32)
-        out_ref = oracle.moe_tokens(x, ref["topk_idx"], ref["topk_w"], lay.routed, lay.shared, toks)
-        assert_output_close(y_to_f64(y)[toks], out_ref, f"{name} chunk {ci}")
-
-
 def test_decode_t1_layer_steps():
     wl = configs.WORKLOADS["decode_t1_d2048"]
     sh = wl.shape
