@@ -118,7 +118,7 @@ static RouteArgs route_args(const moe_shape* s, const uint16_t* x, const uint16_
                             const moe_routing* rt, void* ws, const Opts& o) {
     RouteArgs a{};
     a.T = s->T; a.d = s->d; a.E = s->E; a.k = s->k; a.I = s->I; a.tile_rows = o.tile_rows;
-    a.gu_rows = o.gemm_rows; a.dn_rows = o.gemm_rows;
+    a.gu_rows = o.gemm_rows; a.dn_rows = o.gemm_rows < kDnMaxRows ? o.gemm_rows : kDnMaxRows;
     a.x = x; a.w_router = wr; a.bias = bias;
     a.topk_idx = rt->topk_idx_dev; a.topk_w = rt->topk_w_dev; a.counts = rt->counts_dev;
     a.offsets = rt->offsets_dev; a.perm = rt->perm_dev; a.pos = rt->pos_dev; a.tiles = rt->tiles_dev;

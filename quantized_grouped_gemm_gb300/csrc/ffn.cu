@@ -75,7 +75,6 @@ constexpr int kTmThreads = (kTmMmaWarp + 2) * 32;
 constexpr int kTmBox = 16;                    // token rows per small TMA box
 constexpr int kTmBoxL = 64;                   // token rows per large TMA box
 constexpr int kTmKD = 8;                      // "K block done" barriers
-constexpr int kTmXBytes = kMaxN * 128;        // token rows of one K block: 128 rows x 64 bf16
 
 // Ring chunk of the bf16-weight ablation (moe_options.unfused_dequant): the two 128-row
 // matrices of a K block as dequantised bf16, [matrix][16-byte word w4][row][16 bytes], so the
@@ -84,15 +83,19 @@ constexpr int kBf16PairBytes = 2 * kTileRows * kBK * 2;
 
 template <bool kDown, bool kBf16 = false>
 struct TmCfg {
-    // TMEM: A ring of A slots x 64 columns from column 0, then NDS accumulator slots of 128
-    // columns from column DCOL0
+    // TMEM: A ring of A slots x 64 columns from column 0, then NDS accumulator slots of DW
+    // columns from column DCOL0.  Down: four slots of 96 columns, one matrix each, so the two
+    // matrices of the next tile never wait for the epilogue of the current one (token blocks of
+    // at most kDnMaxRows rows)
     static constexpr int A = kDown ? 2 : 4;
-    static constexpr int NDS = kDown ? 3 : 2;
+    static constexpr int NDS = kDown ? 4 : 2;
+    static constexpr uint32_t DW = kDown ? 96u : 128u;
     static constexpr uint32_t DCOL0 = 64u * A;
-    static_assert(DCOL0 + 128u * NDS == 512u, "TMEM columns");
+    static_assert(DCOL0 + DW * NDS == 512u, "TMEM columns");
+    static_assert(!kDown || kDnMaxRows <= (int)DW, "down token block wider than its accumulator slot");
     static constexpr int RX = kDown ? (kBf16 ? 2 : 4) : 8;   // token-row ring slots
     static constexpr int CH = kBf16 ? kBf16PairBytes : kChunkPairBytes;   // bytes of a weight chunk
-    static constexpr int RC = kBf16 ? (kDown ? 4 : 2) : (kDown ? 6 : 8);  // weight-chunk ring slots
+    static constexpr int RC = kBf16 ? 2 : (kDown ? 6 : 8);  // weight-chunk ring slots
     // The two dequant sets take alternate K blocks.  With an even ring every slot belongs to
     // one set, whose parity waits on it are then never more than one phase ahead.  With an odd
     // ring consecutive uses of a slot alternate between the sets: a set reaching block it has
@@ -101,19 +104,24 @@ struct TmCfg {
     // pass a phase early, and the ring's barriers fall out of step.
     static_assert(RC % 2 == 0 || RC >= A + 2, "weight-chunk ring: even, or at least A + 2 slots");
     static constexpr int PARTS = kDown ? 2 : 1;              // hi, lo halves of h
-    static constexpr int XS = PARTS * kTmXBytes;             // bytes of a token-row slot
-    // staging of 32 tokens: gate/up bf16 [32][hi 128 | lo 128]; down two buffers of fp32 [32][128]
-    static constexpr int STAGE = kDown ? 2 * 32 * 512 : 32 * 512;
+    static constexpr int XPART = (kDown ? kDnMaxRows : kMaxN) * 128;   // bytes of one part of a slot
+    static constexpr int XS = PARTS * XPART;                 // bytes of a token-row slot
+    // staging of 32 tokens: gate/up bf16 [32][hi 128 | lo 128]; down a ring of NSTG buffers of
+    // fp32 [32][256] (both matrices of a tile)
+    static constexpr int NSTG = kDown ? 2 : 1;
+    static constexpr int STAGE = kDown ? NSTG * 32 * 1024 : 32 * 512;
+    // bits of a lane's issue history that may still read a staging buffer: the last NSTG - 2 chunks
+    static constexpr uint32_t HIST_MASK = NSTG >= 2 ? (1u << (NSTG >= 2 ? NSTG - 2 : 0)) - 1u : 0u;
     static constexpr int x_off = 0;
     static constexpr int c_off = x_off + RX * XS;
     static constexpr int stage_off = c_off + RC * CH;
-    static constexpr int tab_off = stage_off + STAGE;        // down: float weight[128], int token[128]
-    static constexpr int bar_off = tab_off + 1024;
+    static constexpr int tab_off = stage_off + STAGE;        // down: float weight[2][128], int token[2][128]
+    static constexpr int bar_off = tab_off + 2048;
 };
 
 struct TmBars {
     uint64_t c_full[8], c_empty[8], ready[kTmKD], kb_done[kTmKD];
-    uint64_t d_full[3], d_empty[3], drain[2];
+    uint64_t d_full[4], d_empty[4], drain[2];
     uint32_t tmem_slot;
     int abort;
 };
@@ -224,8 +232,9 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssr
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Wait until at most N of this thread's most recent bulk groups still read their source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <bool kDown, bool kBf16>
@@ -306,7 +315,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                 const int xrow0 = kDown ? (e < p.E ? row0 : p.k * p.T + row0) : row0;
                 const CUtensorMap* tms = (kDown || e < p.E) ? &tm_a : &tm_b;
                 const CUtensorMap* tml = (kDown || e < p.E) ? &tm_al : &tm_bl;
-                const int lo_off = down_stacked(N) ? N * 128 : kTmXBytes;
+                const int lo_off = down_stacked(N) ? N * 128 : C::XPART;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int xs = it % C::RX;
                     if (it >= (uint32_t)C::RX) {
@@ -348,20 +357,20 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                 const bool stacked = kDown && down_stacked(N);   // hi and lo rows as one B operand of 2N rows
                 const uint32_t idesc = idesc_bf16_f32(128, stacked ? 2 * N : N);
                 // gate/up: one or two slots per tile (d_slots); down: use j = 2 tcount + m of the
-                // slot ring, slot j % 3, phase j / 3 (matrices of consecutive tiles take turns, so a
-                // matrix's next slot was drained one matrix earlier)
+                // slot ring, slot j % 4, phase j / 4 (the next tile's two matrices take the two
+                // slots the current tile does not use)
                 const DSlots ds = d_slots(sc, N, kDown);
                 const uint32_t dj = 2 * tcount + m;
-                const int dsl = kDown ? (int)(dj % 3) : 0;
+                const int dsl = kDown ? (int)(dj % 4) : 0;
                 if (kDown) {
-                    if (!mbar_wait(&b->d_empty[dsl], ((dj / 3) & 1) ^ 1, abort)) { ok = false; break; }
+                    if (!mbar_wait(&b->d_empty[dsl], ((dj / 4) & 1) ^ 1, abort)) { ok = false; break; }
                 } else if (!mbar_wait(&b->d_empty[ds.s0], (use[ds.s0] & 1) ^ 1, abort) ||
                            (ds.two && !mbar_wait(&b->d_empty[ds.s1], (use[ds.s1] & 1) ^ 1, abort))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dm = tmem + (kDown ? C::DCOL0 + 128u * dsl : (m ? ds.col1 : ds.col0));
+                const uint32_t dm = tmem + (kDown ? C::DCOL0 + C::DW * dsl : (m ? ds.col1 : ds.col0));
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int as = it % C::A, xs = it % C::RX;
                     if (!mbar_wait(&b->ready[it % kTmKD], (it / kTmKD) & 1, abort)) { ok = false; break; }
@@ -379,7 +388,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                         for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
                             for (int part = 0; part < C::PARTS; ++part)
-                                tc_mma_bf16_ts(dm, a0 + 8u * ks, xd + (uint64_t)((part * kTmXBytes + ks * 32) >> 4), idesc,
+                                tc_mma_bf16_ts(dm, a0 + 8u * ks, xd + (uint64_t)((part * C::XPART + ks * 32) >> 4), idesc,
                                                (kb | ks | part) ? 1u : 0u);
                         }
                     }
@@ -465,20 +474,23 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         // tile of Y are one contiguous block).
         const int q = warp & 3, half = (warp - kTmEpiWarp0) >> 2, r = 32 * q + lane, et = threadIdx.x - kTmEpiWarp0 * 32;
         uint8_t* stage = smem + C::stage_off;
-        float* s_w = reinterpret_cast<float*>(smem + C::tab_off);
-        int* s_tok = reinterpret_cast<int*>(smem + C::tab_off + 512);
+        float* s_w = reinterpret_cast<float*>(smem + C::tab_off);          // [2][128]
+        int* s_tok = reinterpret_cast<int*>(smem + C::tab_off + 1024);     // [2][128]
         const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
         const size_t yrows = (size_t)(p.k + 1) * p.T;
         uint32_t tcount = 0, chunk = 0, sc = 0, use[3] = {0, 0, 0};
+        uint32_t hist = 0;   // down: bit i = this lane committed a bulk operation i + 1 chunks ago
         bool ok = true;
         for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x, ++tcount) {
             const int4 t = p.tiles[tile];
             const int e = t.x, row0 = t.y, rows = t.z, wt = t.w, N = tile_n(rows);
             const size_t orow0 = e < p.E ? (size_t)row0 : (size_t)p.k * p.T + row0;   // row of H / Y
             if (kDown && et < rows) {
+                // tables of this tile, double-buffered by tile parity: the previous tile's last
+                // bulk issues (after its last barrier) may still read the other half
                 const int asg = e < p.E ? p.perm[row0 + et] : 0;
-                s_w[et] = e < p.E ? p.topk_w[asg] : 1.0f;
-                s_tok[et] = e < p.E ? asg / p.k : row0 + et;
+                s_w[128 * (tcount & 1) + et] = e < p.E ? p.topk_w[asg] : 1.0f;
+                s_tok[128 * (tcount & 1) + et] = e < p.E ? asg / p.k : row0 + et;
             }
             if (!kDown) {
                 const DSlots ds = d_slots(sc, N, false);
@@ -538,71 +550,108 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                 if (ds.two) use[ds.s1]++;
                 sc += ds.two ? 2 : 1;
             } else {
-                // down: matrix 0 (output rows 256 wt ..) is drained and its slot released before
-                // matrix 1, so the next tile's MMAs into matrix 0 start half an epilogue earlier
+                // down: wait for both accumulators of the tile (matrices m = 0, 1: output rows
+                // 256 wt + 128 m ..), then per chunk of 32 tokens: weight * y of both matrices from
+                // TMEM into a staging buffer [32][256] (a token's 256 outputs contiguous), one
+                // barrier, and one 1 KB bulk reduce-add per token (or one row copy per chunk).  The
+                // two slots are released once their last chunk has been read; the next chunk's TMEM
+                // loads are issued before the barrier, so their latency overlaps the barrier and the
+                // bulk issues.  A staging buffer is written again NSTG chunks later: before each
+                // barrier the issuing lanes wait until their operations of NSTG - 1 chunks back have
+                // read it.
                 if (et == 0) TM_TRACE(TT_ET, tcount);
                 const bool stacked = down_stacked(N);   // the lo half's products sit N columns further
-                for (int m = 0; m < 2; ++m) {
-                    const uint32_t dj = 2 * tcount + m;   // use j of the slot ring: slot j % 3, phase j / 3
-                    const int dsl = (int)(dj % 3);
-                    bool failed = false;
-                    if (et == 0 && !mbar_wait(&b->d_full[dsl], (dj / 3) & 1, abort)) {
-                        tm_abort(abort, p.status);
-                        failed = true;
-                    }
-                    // (also: the weight / token tables are written); one decision for all warps
-                    if (named_bar_or(2, kTmEpiThreads, failed || *abort != 0)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t td = tlane + C::DCOL0 + 128u * dsl;
-                    for (int c0 = 0; c0 < N; c0 += 32, ++chunk) {
-                        const int c = c0 + 16 * half;          // this warp's 16 tokens: c .. c+15
-                        const bool last = c0 + 32 >= N;
-                        // two staging buffers, alternate chunks: a chunk's bulk operations read one
-                        // while the next chunk is written into the other
-                        float* st = reinterpret_cast<float*>(stage) + (chunk & 1) * (32 * 128);   // [32][128]
-                        uint32_t R[16], L[16];
-                        if (c < N) {
-                            tmem_ld16(td + c, R);
-                            if (stacked) tmem_ld16(td + N + c, L);
-                            tmem_ld_wait();
-                        }
-                        if (last) {   // this accumulator is no longer read: its slot is free
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&b->d_empty[dsl]);
-                        }
-                        if (c < N) {
+                const float* tw = s_w + 128 * (tcount & 1);
+                const int* ttok = s_tok + 128 * (tcount & 1);
+                const int n_me = (warp - kTmEpiWarp0) + 8 * lane;   // reduce-adds: this lane's token
+                const uint32_t j0 = 2 * tcount;   // uses j0, j0 + 1 of the slot ring: slot j % 4, phase j / 4
+                const int sl0 = (int)(j0 % 4), sl1 = (int)((j0 + 1) % 4);
+                bool failed = false;
+                if (et == 0 && (!mbar_wait(&b->d_full[sl0], (j0 / 4) & 1, abort) ||
+                                !mbar_wait(&b->d_full[sl1], ((j0 + 1) / 4) & 1, abort))) {
+                    tm_abort(abort, p.status);
+                    failed = true;
+                }
+                // (also: the weight / token tables are written); one decision for all warps
+                if (named_bar_or(2, kTmEpiThreads, failed || *abort != 0)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t td0 = tlane + C::DCOL0 + C::DW * sl0, td1 = tlane + C::DCOL0 + C::DW * sl1;
+                uint32_t R0[16], R1[16];
+                if (16 * half < N) {
+                    tmem_ld16(td0 + 16 * half, R0);
+                    tmem_ld16(td1 + 16 * half, R1);
+                    if (stacked) {   // one chunk: y = hi products + lo products, summed right away
+                        uint32_t L[16];
+                        tmem_ld16(td0 + N + 16 * half, L);
+                        tmem_ld_wait_regs(R0);
+                        tmem_ld_wait_regs(L);
 #pragma unroll
-                            for (int u = 0; u < 16; ++u) {
-                                const float w = c + u < rows ? s_w[c + u] : 0.0f;
-                                const float y = __uint_as_float(R[u]) + (stacked ? __uint_as_float(L[u]) : 0.0f);
-                                st[(16 * half + u) * 128 + r] = w * y;
-                            }
-                        }
-                        fence_proxy_async_smem();
-                        named_bar_sync(2, kTmEpiThreads);
-                        const int nv = rows - c0 < 32 ? rows - c0 : 32;   // rows of this chunk
-                        if (p.rows_out) {
-                            if (et == 0) {
-                                bulk_s2g(p.Y + ((size_t)(2 * wt + m) * yrows + orow0 + c0) * 128, st, (uint32_t)nv * 512);
-                                bulk_commit();
-                                bulk_wait_read1();   // the previous chunk (the other buffer) has been read
-                            }
-                        } else if (lane < 4) {
-                            // token n = (epilogue warp) + 8 lane: its 512-byte row piece added into
-                            // acc; the issues are spread over the eight warps
-                            const int n = (warp - kTmEpiWarp0) + 8 * lane;
-                            if (n < nv) {
-                                bulk_reduce_add_f32(p.acc + (size_t)s_tok[c0 + n] * p.d + (size_t)wt * 256 + 128 * m,
-                                                    st + n * 128, 512);
-                                bulk_commit();
-                                bulk_wait_read1();   // this lane's previous chunk has been read
-                            } else {
-                                bulk_wait_read0();
-                            }
-                        }
-                        named_bar_sync(2, kTmEpiThreads);
+                        for (int u = 0; u < 16; ++u)
+                            R0[u] = __float_as_uint(__uint_as_float(R0[u]) + __uint_as_float(L[u]));
+                        tmem_ld16(td1 + N + 16 * half, L);
+                        tmem_ld_wait_regs(R1);
+                        tmem_ld_wait_regs(L);
+#pragma unroll
+                        for (int u = 0; u < 16; ++u)
+                            R1[u] = __float_as_uint(__uint_as_float(R1[u]) + __uint_as_float(L[u]));
                     }
+                }
+                for (int c0 = 0; c0 < N; c0 += 32, ++chunk) {
+                    const int c = c0 + 16 * half;          // this warp's 16 tokens: c .. c+15
+                    const bool last = c0 + 32 >= N;
+                    float* st = reinterpret_cast<float*>(stage) + (chunk % C::NSTG) * (32 * 256);   // [32][256]
+                    if (c < N && !stacked) {
+                        tmem_ld_wait_regs(R0);
+                        tmem_ld_wait_regs(R1);
+                    }
+                    if (last) {   // both accumulators are no longer read: their slots are free
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(&b->d_empty[sl0]);
+                            mbar_arrive(&b->d_empty[sl1]);
+                        }
+                    }
+                    if (c < N) {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const float w = c + u < rows ? tw[c + u] : 0.0f;
+                            st[(16 * half + u) * 256 + r] = w * __uint_as_float(R0[u]);
+                            st[(16 * half + u) * 256 + 128 + r] = w * __uint_as_float(R1[u]);
+                        }
+                    }
+                    if (c + 32 < N) {   // the next chunk (never stacked)
+                        tmem_ld16(td0 + c + 32, R0);
+                        tmem_ld16(td1 + c + 32, R1);
+                    }
+                    fence_proxy_async_smem();
+                    const int nv = rows - c0 < 32 ? rows - c0 : 32;   // rows of this chunk
+                    if (p.rows_out ? et < 2 : lane < 4) {   // issuing lanes: chunk - (NSTG - 1) has been read
+                        const int pend = __popc(hist & C::HIST_MASK);
+                        if (pend >= 2) bulk_wait_read<2>();
+                        else if (pend == 1) bulk_wait_read<1>();
+                        else bulk_wait_read<0>();
+                    }
+                    named_bar_sync(2, kTmEpiThreads);
+                    uint32_t issued = 0;
+                    if (p.rows_out) {
+                        // rows of Y [d/128][(k+1)T][128]: the chunk's rows of one 128-column tile are
+                        // one contiguous block (thread et = matrix m copies its half of the staging);
+                        // the staging rows hold 256 floats, so the copy runs row by row
+                        if (et < 2) {
+                            float* ydst = p.Y + ((size_t)(2 * wt + et) * yrows + orow0 + c0) * 128;
+                            for (int n = 0; n < nv; ++n) bulk_s2g(ydst + (size_t)n * 128, st + n * 256 + 128 * et, 512);
+                            bulk_commit();
+                            issued = 1;
+                        }
+                    } else if (lane < 4 && n_me < nv) {
+                        // token n = (epilogue warp) + 8 lane: its 1 KB row piece added into acc; the
+                        // issues are spread over the eight warps
+                        bulk_reduce_add_f32(p.acc + (size_t)ttok[c0 + n_me] * p.d + (size_t)wt * 256, st + n_me * 256, 1024);
+                        bulk_commit();
+                        issued = 1;
+                    }
+                    hist = (hist << 1) | issued;
                 }
             }
             if (et == 0) TM_TRACE(TT_ED, tcount);

@@ -81,6 +81,9 @@ constexpr int kDecodeMaxT = 8;          // largest T the decode (GEMV) kernels t
 // allow, and every block re-reads its expert's weights).  The workspace's tile lists are sized
 // for the smallest block.
 constexpr int kGemmRowsDefault = 128;
+// The down projection caps its blocks at 96 rows: four 96-column accumulator slots then hold two
+// tiles (two matrices each), so a tile's MMAs never wait for the previous tile's epilogue.
+constexpr int kDnMaxRows = 96;
 constexpr int kGemmRowsMin = 16;
 inline bool gemm_rows_valid(int r) { return r == 16 || r == 32 || r == 64 || r == 128; }
 
@@ -382,6 +385,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The same wait with the loaded registers as operands: arithmetic on them cannot be scheduled
+// before it (needed when other code sits between a tcgen05.ld and its wait).
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
 
 // 32 lanes x 32 bits x 32 columns (one column per register) into TMEM.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {

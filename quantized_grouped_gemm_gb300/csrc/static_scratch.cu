@@ -113,7 +113,8 @@ extern "C" int moe_forward_decode_static(const moe_shape* s, const uint16_t* x, 
 
     RouteArgs ra{};
     ra.T = 1; ra.d = s->d; ra.E = s->E; ra.k = s->k; ra.I = s->I; ra.tile_rows = 32;
-    ra.gu_rows = ra.dn_rows = kGemmRowsDefault;
+    ra.gu_rows = kGemmRowsDefault;
+    ra.dn_rows = kDnMaxRows;
     ra.x = x; ra.w_router = w_router; ra.bias = logit_bias;
     ra.topk_idx = rt->topk_idx_dev; ra.topk_w = rt->topk_w_dev; ra.counts = rt->counts_dev;
     ra.offsets = rt->offsets_dev; ra.perm = rt->perm_dev; ra.pos = rt->pos_dev; ra.tiles = rt->tiles_dev;
