@@ -14,9 +14,10 @@ with its own roofline, end-to-end number and oracle baseline (N=1 only).
 
 Timing: W warm-up steps (the first runs eagerly, the rest as the timed steps run), then exactly
 K steps between CUDA events on the launching stream, barrier + synchronize on both sides, max
-over ranks.  Prefill steps replay from CUDA graphs of the library calls, 8 steps per graph;
-every 8th block of 8 steps runs phase by phase (one graph per phase, events in between), which
-gives the per-kernel times of the roofline; a last partial block runs step by step.  Without
+over ranks.  Prefill steps replay from CUDA graphs of the library calls, 8 steps per graph; the
+first step of every 4th block of 8 runs phase by phase (one graph per phase, events in between),
+which gives the per-kernel times of the roofline, and the rest of that block, like a last
+partial block, runs one graph per step.  Without
 --steps, K is chosen for about 1.5 s of timed work (the calibration steps count as warm-up).
 Multi-GPU (torchrun): every rank runs its own rotation of the chunks (weak scaling, no
 collective on the data path).
@@ -175,14 +176,15 @@ def algorithmic_counts(shp, counts):
 
 
 def step_plan(n, multi, probe_every=None):
-    """How n consecutive steps run: blocks of `multi` steps replay one graph ("multi"); every
-    probe_every-th block runs its steps phase by phase with events in between ("probe"); a last
-    partial block runs step by step ("single").  Entries: (kind, first step)."""
+    """How n consecutive steps run: blocks of `multi` steps replay one graph ("multi"); the first
+    step of every probe_every-th block runs phase by phase with events in between ("probe") and
+    the rest of that block step by step ("single", one graph per step), as does a last partial
+    block.  Entries: (kind, first step)."""
     ops, s, b = [], 0, 0
     while s < n:
         m = min(multi, n - s)
         if probe_every and b % probe_every == 0:
-            ops += [("probe", s + j) for j in range(m)]
+            ops += [("probe", s)] + [("single", s + j) for j in range(1, m)]
         elif m == multi:
             ops.append(("multi", s))
         else:
@@ -257,7 +259,7 @@ def run_ours(wname, args, rank, world, local, headline=True):
     stream = torch.cuda.Stream(device=dev)
     opts = moe.options()
     W = max(1, args.warmup)
-    PROBE = 8
+    PROBE = 4      # the first step of every 4th block of MULTI steps is timed phase by phase
 
     # ---- warm-up step 1 runs eagerly (the library's one-time set-up: kernel attributes, the
     # one-launch decode kernel's occupancy check); then the graphs are captured
@@ -287,14 +289,16 @@ def run_ours(wname, args, rank, world, local, headline=True):
                 f()
             stream.synchronize()
             # per set: the four phases as separate graphs (probe steps run these with events in
-            # between, for the kernel times); and MULTI consecutive steps (a multiple of the set
-            # count) as one graph, in which consecutive kernels, also across steps, overlap their
-            # prologues through programmatic dependent launch
-            graphs = []
+            # between, for the kernel times), the whole step as one graph, and MULTI consecutive
+            # steps (a multiple of the set count) as one graph; inside a graph consecutive
+            # kernels, also across steps, overlap their prologues through programmatic dependent
+            # launch
+            graphs, step_graphs = [], []
             for gi in range(nsets):
                 n0 = moe.moe_launch_count()
                 gc = []
-                for f in calls_for(L[gi % layers], xs[gi % len(xs)]):
+                calls = calls_for(L[gi % layers], xs[gi % len(xs)])
+                for f in calls:
                     g = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g, stream=stream):
                         f()
@@ -302,6 +306,11 @@ def run_ours(wname, args, rank, world, local, headline=True):
                 if gi == 0:
                     launches_per_step = moe.moe_launch_count() - n0
                 graphs.append(gc)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for f in calls:
+                        f()
+                step_graphs.append(g)
             MULTI = nsets * -(-8 // nsets)
             multi = torch.cuda.CUDAGraph()
             with torch.cuda.graph(multi, stream=stream):
@@ -312,7 +321,7 @@ def run_ours(wname, args, rank, world, local, headline=True):
 
     probes = []   # per probe step: [route, gate/up, down, combine] ms
 
-    def run(n, with_probes):
+    def run(n, with_probes, keep=True):
         for kind, s in step_plan(n, MULTI, PROBE if with_probes else None):
             if decode:
                 x_in.copy_(x_all[s % nsteps_x:s % nsteps_x + 1], non_blocking=True)
@@ -320,21 +329,21 @@ def run_ours(wname, args, rank, world, local, headline=True):
             elif kind == "multi":
                 multi.replay()
             elif kind == "single":
-                for gph in graphs[s % len(graphs)]:
-                    gph.replay()
+                step_graphs[s % len(step_graphs)].replay()
             else:
                 ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
                 ev[0].record(stream)
                 for i, gph in enumerate(graphs[s % len(graphs)]):
                     gph.replay()
                     ev[i + 1].record(stream)
-                probes.append(ev)
+                if keep:
+                    probes.append(ev)
 
     dist = None
     if world > 1:
         import torch.distributed as dist
     with torch.cuda.stream(stream):
-        run(W - 1, False)
+        run(W - 1, True, keep=False)   # the same mix of graphs as the timed steps
         stream.synchronize()
         warmup_steps = W
         if args.steps is None:       # auto: about 1.5 s of timed work (these steps count as warm-up)

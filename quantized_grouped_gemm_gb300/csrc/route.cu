@@ -496,11 +496,53 @@ __device__ __forceinline__ int block_exclusive_scan256(int v, int* s_tmp) {
     return base + x - v;
 }
 
+// The expert owning entry t of a list whose per-expert entry counts have the exclusive scan
+// sc[0..256] (sc[256] = total, t < total): the largest e with sc[e] <= t, which has sc[e + 1] > t.
+__device__ __forceinline__ int scan_owner(const int* sc, int t) {
+    int lo = 0, hi = 256;
+#pragma unroll
+    for (int step = 0; step < 8; ++step) {
+        const int mid = (lo + hi) >> 1;
+        if (sc[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// All n entries of a GEMM tile list, written by the CTA's threads: position j holds the shared
+// expert's entry j - from when from <= j < from + nsh * mt, else routed entry jj (jj = j before
+// the shared block, j - nsh * mt after it) = (token block jj / mt, weight tile jj % mt) of the
+// routed experts' blocks in expert order (sb: exclusive scan of their block counts).  An
+// expert's cnt rows from off are cut into nb near-equal blocks: block i has q + (i < r) rows
+// (q = cnt / nb, r = cnt % nb) and starts at off + i q + min(i, r); the shared expert cuts the
+// T token rows the same way into nsh blocks.  Entry = (expert, first row, rows, weight tile).
+__device__ void gemm_list_entries(int4* list, int n, int mt, int nsh, int from, const int* sb, const int* cnt,
+                                  const int* off, int T, int E) {
+    const int nsh_e = nsh * mt;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        int ex, i, m, rows, nb, r0;
+        if (j >= from && j < from + nsh_e) {
+            const int q = j - from;
+            ex = E; i = q / mt; m = q % mt; rows = T; nb = nsh; r0 = 0;
+        } else {
+            const int jj = j < from ? j : j - nsh_e;
+            const int blk = jj / mt;
+            m = jj % mt;
+            ex = scan_owner(sb, blk);
+            i = blk - sb[ex];
+            rows = cnt[ex]; nb = sb[ex + 1] - sb[ex]; r0 = off[ex];
+        }
+        const int q = rows / nb, r = rows % nb;
+        list[j] = make_int4(ex, r0 + i * q + min(i, r), q + (i < r ? 1 : 0), m);
+    }
+}
+
 __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     __shared__ int s_tmp[8];
-    __shared__ int s_tot[4];   // [0] block-map tiles, [1] gate/up blocks, [2] down blocks
     __shared__ int s_part[4][256];
     __shared__ int s_off[256];
+    __shared__ int s_cnt[256];
+    __shared__ int s_tb[257], s_gb[257], s_db[257];   // exclusive scans: block-map tiles, GEMM blocks
     pdl_wait();
     pdl_launch_dependents();
     const int E = 256;
@@ -558,71 +600,58 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
             blk_counts[(size_t)b * E + e] = 0;
         }
     }
-    if (part != 0) return;          // warps 8..31 are done; the rest uses named barrier 1 (256 threads)
-    const int off = s_off[e];
-
-    // exported block map: ceil(count / tile_rows) tiles per expert, expert-ascending
-    const int BM = a.tile_rows;
-    const int nt = (run + BM - 1) / BM;
-    const int tbase = block_exclusive_scan256(nt, s_tmp);
-    for (int i = 0; i < nt; ++i) {
-        int32_t* tt = a.tiles + 3 * (size_t)(tbase + i);
-        tt[0] = e;
-        tt[1] = off + i * BM;
-        tt[2] = min(BM, run - i * BM);
+    // per expert: tiles of the exported block map and token blocks of the two GEMM tile lists,
+    // and their exclusive scans over the experts (warps 0..7, named barrier 1)
+    if (part == 0) {
+        s_cnt[e] = run;
+        const int nt = (run + a.tile_rows - 1) / a.tile_rows;
+        const int nn = (run + a.gu_rows - 1) / a.gu_rows;
+        const int nd = (run + a.dn_rows - 1) / a.dn_rows;
+        const int tb = block_exclusive_scan256(nt, s_tmp);
+        s_tb[e] = tb;
+        if (e == E - 1) s_tb[E] = tb + nt;
+        named_bar_sync(1, 256);
+        const int gb = block_exclusive_scan256(nn, s_tmp);
+        s_gb[e] = gb;
+        if (e == E - 1) s_gb[E] = gb + nn;
+        named_bar_sync(1, 256);
+        const int db = block_exclusive_scan256(nd, s_tmp);
+        s_db[e] = db;
+        if (e == E - 1) s_db[E] = db + nd;
     }
-    if (e == E - 1) s_tot[0] = tbase + nt;
+    __syncthreads();
 
+    // Every entry of the three lists is a function of its position, so all threads write them
+    // (an expert's entries are not left to one thread: a heavy expert has hundreds).
+    // Exported block map: ceil(count / tile_rows) tiles per expert, expert-ascending.
+    const int BM = a.tile_rows;
+    const int ntile = s_tb[E];
+    for (int t = threadIdx.x; t < ntile; t += blockDim.x) {
+        const int ex = scan_owner(s_tb, t), i = t - s_tb[ex];
+        int32_t* tt = a.tiles + 3 * (size_t)t;
+        tt[0] = ex;
+        tt[1] = s_off[ex] + i * BM;
+        tt[2] = min(BM, s_cnt[ex] - i * BM);
+    }
     // GEMM tile lists: an expert's rows split into near-equal token blocks of at most
     // a.gu_rows (gate/up) and a.dn_rows (down) rows (moe_options.gemm_rows); each block is
-    // repeated for every weight tile (weight tile innermost, so the CTAs that run at the same time share the block's activation rows
-    // in L2).  The shared expert (expert index E) covers token rows 0..T-1 in full blocks; its
-    // tiles are inserted where the CTAs run one tile fewer (shared_tiles_at), the experts'
-    // tiles follow in expert order around them.
+    // repeated for every weight tile (weight tile innermost, so the CTAs that run at the same
+    // time share the block's activation rows in L2).  The shared expert (expert index E)
+    // covers token rows 0..T-1 in full blocks; its entries sit at positions [from, from + its
+    // count) -- where the persistent CTAs run one tile fewer (shared_tiles_at) -- and the
+    // experts' entries follow in expert order around them.
     const int MTgu = a.I / kTileRows, MTdn = a.d / 256;   // 128 gate+up row pairs; 256-row down tiles
-    const int nn = (run + a.gu_rows - 1) / a.gu_rows;
-    const int nd = (run + a.dn_rows - 1) / a.dn_rows;
     const int nsh = (a.T + a.gu_rows - 1) / a.gu_rows;
     const int nshd = (a.T + a.dn_rows - 1) / a.dn_rows;
-    const int nbase = block_exclusive_scan256(nn, s_tmp);
-    if (e == E - 1) s_tot[1] = nbase + nn;
-    named_bar_sync(1, 256);
-    const int dbase = block_exclusive_scan256(nd, s_tmp);
-    if (e == E - 1) s_tot[2] = dbase + nd;
-    named_bar_sync(1, 256);
-    int4* gu = reinterpret_cast<int4*>(a.ws + a.L.gu_tiles);
-    int4* dn = reinterpret_cast<int4*>(a.ws + a.L.dn_tiles);
-    // nb near-equal blocks of `rows` rows from r0; entry j of block i (entry (base + i) * mt + m
-    // of its own sequence) goes to list position j + (j >= from ? by : 0)
-    auto split = [&](int4* list, int mt, int base, int ex, int r0, int rows, int nb, int from, int by) {
-        const int q = rows / nb, rem = rows % nb;
-        for (int i = 0; i < nb; ++i) {
-            const int n = q + (i < rem ? 1 : 0);
-            for (int m = 0; m < mt; ++m) {
-                const int j = (base + i) * mt + m;
-                list[(size_t)(j >= from ? j + by : j)] = make_int4(ex, r0, n, m);
-            }
-            r0 += n;
-        }
-    };
-    const int shg = nsh * MTgu, shd = nshd * MTdn;   // the shared expert's entries
-    const int pg = shared_tiles_at((nsh + s_tot[1]) * MTgu, shg, a.num_sms);
-    const int pd = shared_tiles_at((nshd + s_tot[2]) * MTdn, shd, a.num_sms);
-    if (nn > 0) split(gu, MTgu, nbase, e, off, run, nn, pg, shg);
-    if (nd > 0) split(dn, MTdn, dbase, e, off, run, nd, pd, shd);
-    // shared expert token blocks (one thread each)
-    for (int i = e; i < nsh; i += E) {
-        const int q = a.T / nsh, rem = a.T % nsh;
-        split(gu, MTgu, i, E, i * q + min(i, rem), q + (i < rem ? 1 : 0), 1, 0, pg);
-    }
-    for (int i = e; i < nshd; i += E) {
-        const int q = a.T / nshd, rem = a.T % nshd;
-        split(dn, MTdn, i, E, i * q + min(i, rem), q + (i < rem ? 1 : 0), 1, 0, pd);
-    }
-    if (e == 0) {
-        *a.num_tiles = s_tot[0];
-        *reinterpret_cast<int32_t*>(a.ws + a.L.gu_num) = (nsh + s_tot[1]) * MTgu;
-        *reinterpret_cast<int32_t*>(a.ws + a.L.dn_num) = (nshd + s_tot[2]) * MTdn;
+    const int ngu = (nsh + s_gb[E]) * MTgu, ndn = (nshd + s_db[E]) * MTdn;
+    const int pg = shared_tiles_at(ngu, nsh * MTgu, a.num_sms);
+    const int pd = shared_tiles_at(ndn, nshd * MTdn, a.num_sms);
+    gemm_list_entries(reinterpret_cast<int4*>(a.ws + a.L.gu_tiles), ngu, MTgu, nsh, pg, s_gb, s_cnt, s_off, a.T, E);
+    gemm_list_entries(reinterpret_cast<int4*>(a.ws + a.L.dn_tiles), ndn, MTdn, nshd, pd, s_db, s_cnt, s_off, a.T, E);
+    if (threadIdx.x == 0) {
+        *a.num_tiles = ntile;
+        *reinterpret_cast<int32_t*>(a.ws + a.L.gu_num) = ngu;
+        *reinterpret_cast<int32_t*>(a.ws + a.L.dn_num) = ndn;
     }
 }
 

@@ -72,4 +72,6 @@ def test_step_plan_runs_exactly_n_steps(n, multi, probe):
     assert steps == list(range(n))
     if probe:
         assert plan[0][0] == "probe"
+        # one probe step per probe block: a small share of the timed steps
+        assert sum(k == "probe" for k, _ in plan) == -(-(-(-n // multi)) // probe)
     assert all(s % multi == 0 for kind, s in plan if kind == "multi")
