@@ -183,7 +183,11 @@ int moe_pack_weights(const moe_shape* shape, const moe_expert_weights* src, int 
  * for moe_grouped_ffn.
  * The logit of (t, e) is fixed bit-exactly: 32 partial fp32 sums, sum l taking
  * k = 256*i + 8*l + j (i ascending, j = 0..7) with fused multiply-adds from 0, then the
- * tree s[i] += s[i+m] for m = 16, 8, 4, 2, 1, then + logit_bias[e]. */
+ * tree s[i] += s[i+m] for m = 16, 8, 4, 2, 1, then + logit_bias[e].
+ * Prefill kernels are launched with programmatic dependent launch; the first two read
+ * w_router_dev before the previous kernel on the stream has finished (everything else only
+ * after it), so w_router_dev must not be written by the kernel launched just before this call
+ * on the same stream. */
 int moe_route(const moe_shape* shape, const uint16_t* x_dev, const uint16_t* w_router_dev,
               const float* logit_bias_dev, const moe_routing* routing, void* workspace_dev,
               size_t workspace_bytes, const moe_options* options, void* stream);

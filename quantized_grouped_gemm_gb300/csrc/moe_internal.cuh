@@ -191,6 +191,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Expect `bytes` more transaction bytes in the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
 // try_wait with a suspend-time hint: the thread sleeps until the phase completes (or the hint
 // runs out) instead of spinning, so waiting warps leave the issue slots to working warps.
 constexpr uint32_t kSuspendHintNs = 1000000;   // 1 ms

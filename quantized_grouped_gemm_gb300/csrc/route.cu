@@ -59,11 +59,12 @@ __device__ __forceinline__ float warp_pinned_logit(const uint16_t* xrow, const u
 }
 
 // ---------------------------------------------------------------------------------------
-// router_wnorm: ||W_r[e]||_2 (fp32) for every expert; one warp per expert.
+// router_wnorm: ||W_r[e]||_2 (fp32) for every expert; one warp per expert.  It reads only the
+// router weight, so it runs before waiting for the previous kernel on the stream (programmatic
+// dependent launch); the wait comes before the result is written, so the launch order of the
+// workspace writes is kept.
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) router_wnorm(RouteArgs a) {
-    pdl_wait();
-    pdl_launch_dependents();
     const int lane = threadIdx.x & 31, e = blockIdx.x * 4 + (threadIdx.x >> 5);
     float s = 0.f;
     for (int c = 8 * lane; c < a.d; c += 256) {
@@ -75,6 +76,8 @@ __global__ void __launch_bounds__(128) router_wnorm(RouteArgs a) {
     }
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    pdl_wait();
+    pdl_launch_dependents();
     if (lane == 0) reinterpret_cast<float*>(a.ws + a.L.wnorm)[e] = sqrtf(s);
 }
 
@@ -116,12 +119,22 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // the router-weight tiles of the first stages do not depend on the previous kernel: they are
+    // requested before the wait (the stage barrier expects their bytes, and the token tiles'
+    // bytes and the producer's arrival after the wait)
+    const int npre = kb1 - kb0 < kRtStages ? kb1 - kb0 : kRtStages;
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_w);
+        for (int i = 0; i < npre; ++i) {
+            mbar_expect_tx(&full[i], kRtB);
+            tma_load_2d(smem + i * (kRtA + kRtB) + kRtA, &tm_w, (kb0 + i) * kBK, 0, &full[i]);
+        }
+    }
     pdl_wait();
     pdl_launch_dependents();
     if (warp == 0) {
         if (lane == 0) {
             prefetch_tmap(&tm_x);
-            prefetch_tmap(&tm_w);
             uint32_t it = 0;
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int st = it % kRtStages;
@@ -130,15 +143,21 @@ __global__ void __launch_bounds__(192, 1)
                     set_status(status, MOE_STATUS_TIMEOUT);
                     break;
                 }
-                mbar_arrive_expect_tx(&full[st], kRtA + kRtB);
                 uint8_t* dst = smem + st * (kRtA + kRtB);
+                if ((int)it < npre) {   // router-weight tile already requested
+                    mbar_arrive_expect_tx(&full[st], kRtA);
+                } else {
+                    mbar_arrive_expect_tx(&full[st], kRtA + kRtB);
+                    tma_load_2d(dst + kRtA, &tm_w, kb * kBK, 0, &full[st]);
+                }
                 tma_load_2d(dst, &tm_x, kb * kBK, blockIdx.x * 128, &full[st]);
-                tma_load_2d(dst + kRtA, &tm_w, kb * kBK, 0, &full[st]);
             }
-            // every issued copy lands before the CTA can exit
+            // every issued copy lands before the CTA can exit (including router-weight tiles
+            // requested before the wait for stages the loop did not reach after a timeout)
             int never = 0;
-            const uint32_t first = it > (uint32_t)kRtStages ? it - kRtStages : 0;
-            for (uint32_t i = first; i < it; ++i) mbar_wait(&full[i % kRtStages], (i / kRtStages) & 1, &never);
+            const uint32_t last = it > (uint32_t)npre ? it : (uint32_t)npre;
+            const uint32_t first = last > (uint32_t)kRtStages ? last - kRtStages : 0;
+            for (uint32_t i = first; i < last; ++i) mbar_wait(&full[i % kRtStages], (i / kRtStages) & 1, &never);
         }
     } else if (warp == 1) {
         if (lane == 0) {
