@@ -48,7 +48,8 @@ constexpr int kFzCluster = 4;         // CTAs per unit: the four column quarters
 constexpr int kFzSlice = 128;         // h rows per unit (one 128-row tile of gate and up)
 constexpr int kFzReplicas = 8;        // copies of the published logit words
 constexpr int kFzMaxUnits = 72;       // (k + 1) * I / 128 for I <= 1024 (grids that fit the GPU at once)
-constexpr int kFzRingMax = 11;        // chunk-pair slots (two CTAs per SM fit)
+constexpr int kFzRingMax = 16;        // chunk-pair slots
+constexpr int kFzOneCtaSmem = 120000; // dynamic shared memory of a CTA: above half of an SM's
 #ifndef MOE_POLL_SLEEP_NS
 #define MOE_POLL_SLEEP_NS 200
 #endif
@@ -589,7 +590,7 @@ __global__ void __launch_bounds__(kFzThreads, 2) decode_fused(FzParams P) {
 // Per (device, shared-memory size, unit count): may the grid run (all clusters resident)?
 struct FzCheck { int dev, smem, units, ok; };
 std::mutex g_fz_mutex;
-FzCheck g_fz_checks[16];
+FzCheck g_fz_checks[32];
 int g_fz_nchecks = 0;
 int g_fz_smem_set[64] = {};
 
@@ -601,18 +602,11 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t st, unsig
     const int units = (a.k + 1) * NS, grid = units * kFzCluster;
     if (units > kFzMaxUnits) return cudaErrorNotSupported;
     const int ndt = a.d / 256, max_items = a.d / 256 + 2 * ((ndt + kFzCluster - 1) / kFzCluster);
-    // two CTAs per SM (the next layer's prologue shares the SM): 116736 bytes each, less the
-    // static shared memory and x
-    const int fit = (int)((116736 - 1024 - 8192 - 2 * (size_t)a.d) / kChunkPairBytes);
-    int ring = max_items < kFzRingMax ? max_items : kFzRingMax;
-    if (ring > fit) ring = fit;
-    if (ring < max_items && ring < 5) return cudaErrorNotSupported;   // refills need 5 slots (see the down rounds)
-    size_t smem = (size_t)ring * kChunkPairBytes + (size_t)a.d * 2;
-#ifdef MOE_FZ_MIN_SMEM
-    if (smem < (size_t)(MOE_FZ_MIN_SMEM)) smem = MOE_FZ_MIN_SMEM;   // tuning: fewer CTAs per SM
-#endif
     if (grid < 32) return cudaErrorNotSupported;   // the grid's warps must cover the E router rows
-    FzParams P{a, NS, ring};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
 
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[2];
@@ -624,38 +618,68 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t st, unsig
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kFzThreads);
-    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
 
-    // every cluster must be resident at once (the grid waits on itself); checked once per size
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
-    int verdict = -1;
-    {
+    // Can every cluster be resident at once with `smem` bytes per CTA (the grid waits on
+    // itself)?  Checked once per (device, size, units).
+    auto fits = [&](size_t smem, int& verdict) -> cudaError_t {
         std::lock_guard<std::mutex> lock(g_fz_mutex);
+        verdict = -1;
         for (int i = 0; i < g_fz_nchecks; ++i)
             if (g_fz_checks[i].dev == dev && g_fz_checks[i].smem == (int)smem && g_fz_checks[i].units == units)
                 verdict = g_fz_checks[i].ok;
-        if (verdict < 0) {
-            if ((int)smem > g_fz_smem_set[dev]) {
-                e = cudaFuncSetAttribute(decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                if (e != cudaSuccess) return e;
-                g_fz_smem_set[dev] = (int)smem;
-            }
-            int nclusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&nclusters, decode_fused, &cfg) != cudaSuccess) {
-                (void)cudaGetLastError();
-                nclusters = 0;
-            }
-            verdict = nclusters >= units ? 1 : 0;
-            if (g_fz_nchecks < 16) g_fz_checks[g_fz_nchecks++] = FzCheck{dev, (int)smem, units, verdict};
+        if (verdict >= 0) return cudaSuccess;
+        if ((int)smem > g_fz_smem_set[dev]) {
+            const cudaError_t er = cudaFuncSetAttribute(decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (er != cudaSuccess) return er;
+            g_fz_smem_set[dev] = (int)smem;
         }
+        cfg.dynamicSmemBytes = smem;
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, decode_fused, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            nclusters = 0;
+        }
+        verdict = nclusters >= units ? 1 : 0;
+        if (g_fz_nchecks < 32) g_fz_checks[g_fz_nchecks++] = FzCheck{dev, (int)smem, units, verdict};
+        return cudaSuccess;
+    };
+    // ring of chunk-pair slots within `budget` bytes of shared memory per CTA (less the static
+    // shared memory and x); the down rounds' refills need 5 slots unless every item fits at once
+    auto ring_for = [&](size_t budget) {
+        const int fit = (int)((budget - 8192 - 2 * (size_t)a.d) / kChunkPairBytes);
+        int r = max_items < kFzRingMax ? max_items : kFzRingMax;
+        if (r > fit) r = fit;
+        return r < max_items && r < 5 ? 0 : r;
+    };
+    // First choice: one CTA of this grid per SM (a CTA that shared its SM with another of the
+    // same layer ran ~1.5 us behind the others and held up the whole layer: 16.2 -> 15.5 us per
+    // layer at d = 2048, I = 512); more than half of an SM's shared memory keeps a second one
+    // out.  Grids with more clusters than fit that way take two CTAs per SM (116736 bytes each).
+    int ring = 0, verdict = 0;
+    size_t smem = 0;
+    const int r1 = ring_for(232448);
+    if (r1 > 0) {
+        smem = (size_t)r1 * kChunkPairBytes + (size_t)a.d * 2;
+        if (smem < (size_t)kFzOneCtaSmem) smem = kFzOneCtaSmem;
+#ifdef MOE_FZ_MIN_SMEM
+        if (smem < (size_t)(MOE_FZ_MIN_SMEM)) smem = MOE_FZ_MIN_SMEM;   // tuning builds
+#endif
+        if ((e = fits(smem, verdict)) != cudaSuccess) return e;
+        ring = r1;
+    }
+    if (!verdict) {
+        const int r2 = ring_for(116736);
+        if (r2 == 0) return cudaErrorNotSupported;
+        smem = (size_t)r2 * kChunkPairBytes + (size_t)a.d * 2;
+        if ((e = fits(smem, verdict)) != cudaSuccess) return e;
+        ring = r2;
     }
     if (!verdict) return cudaErrorNotSupported;
+    FzParams P{a, NS, ring};
+    cfg.dynamicSmemBytes = smem;
     cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, decode_fused, P);
     *launches += 1;
