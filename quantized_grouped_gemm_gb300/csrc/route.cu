@@ -570,8 +570,18 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     int32_t* blk_base = blk_counts + (size_t)a.L.nblk * E;
     const int nb = a.L.nblk, nq = (nb + 3) / 4;
     const int b0 = min(nb, part * nq), b1 = min(nb, b0 + nq);
+    // Up to kScanRegs blocks per thread (T <= 4096) are loaded once, all in flight, and kept in
+    // registers for the per-block bases; longer chunks read their counts twice in batches of 8.
+    constexpr int kScanRegs = 32;
+    const bool in_regs = nq <= kScanRegs;
+    int creg[kScanRegs];
     int sum = 0;
-    {
+    if (in_regs) {
+#pragma unroll
+        for (int u = 0; u < kScanRegs; ++u) creg[u] = b0 + u < b1 ? blk_counts[(size_t)(b0 + u) * E + e] : 0;
+#pragma unroll
+        for (int u = 0; u < kScanRegs; ++u) sum += creg[u];
+    } else {
         int b = b0;
         for (; b + 8 <= b1; b += 8) {
             int c[8];
@@ -597,8 +607,19 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
         if (e == E - 1) a.offsets[E] = off + run;
     }
     __syncthreads();
-    // per-block bases: offsets[e] + counts of e in earlier blocks
-    {
+    // per-block bases: offsets[e] + counts of e in earlier blocks; the counts are cleared (the
+    // next call adds into zeros)
+    if (in_regs) {
+        int r = s_off[e] + pre;
+#pragma unroll
+        for (int u = 0; u < kScanRegs; ++u) {
+            if (b0 + u < b1) {
+                blk_base[(size_t)(b0 + u) * E + e] = r;
+                blk_counts[(size_t)(b0 + u) * E + e] = 0;
+            }
+            r += creg[u];
+        }
+    } else {
         int r = s_off[e] + pre;
         int b = b0;
         for (; b + 8 <= b1; b += 8) {
@@ -609,7 +630,7 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
             for (int u = 0; u < 8; ++u) {
                 blk_base[(size_t)(b + u) * E + e] = r;
                 r += c[u];
-                blk_counts[(size_t)(b + u) * E + e] = 0;   // the next call adds into zeros
+                blk_counts[(size_t)(b + u) * E + e] = 0;
             }
         }
         for (; b < b1; ++b) {
