@@ -152,9 +152,15 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------- work
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a workload's
-# dominant kernel, from an ncu capture of the current kernels: {workload: (kernel, bytes)}.
-# Empty until the kernels are captured again after a change (then the line reports null).
-TRAFFIC_BYTES = {}
+# dominant kernel, from an ncu full capture of the current kernels (profiles/ncu_*.md):
+# {workload: (kernel, bytes)}.  A workload whose dominant kernel differs, or is not listed,
+# reports null.
+TRAFFIC_BYTES = {
+    "skew_t16384_d2048": ("down", 122.412032e6 + 3.427584e6),
+    "prefill_t4096_d2048": ("gate_up", 454.353408e6 + 62.073344e6),
+    "prefill_t512_d2048": ("gate_up", 322.279936e6 + 10.222336e6),
+    "decode_t1_d2048": ("decode", 17.078528e6),
+}
 
 
 def algorithmic_counts(shp, counts):
