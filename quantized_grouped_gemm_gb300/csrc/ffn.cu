@@ -347,38 +347,41 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             tm_drain(b->ready, kTmKD, C::RX, it);   // the token rows of the last RX blocks have landed
         }
     } else if (warp >= kTmMmaWarp) {
-        if (lane == 0) {
-            const int m = warp - kTmMmaWarp;   // this thread's accumulator D_m and A matrix m
-            uint32_t it = 0, tcount = 0, sc = 0, use[3] = {0, 0, 0};
-            bool ok = true;
-            const uint64_t xdesc0 = sw128_desc(smem_u32(xring));   // start address advances 16 B per unit
-            for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x, ++tcount) {
-                const int N = tile_n(p.tiles[tile].z);
-                const bool stacked = kDown && down_stacked(N);   // hi and lo rows as one B operand of 2N rows
-                const uint32_t idesc = idesc_bf16_f32(128, stacked ? 2 * N : N);
-                // gate/up: one or two slots per tile (d_slots); down: use j = 2 tcount + m of the
-                // slot ring, slot j % 4, phase j / 4 (the next tile's two matrices take the two
-                // slots the current tile does not use)
-                const DSlots ds = d_slots(sc, N, kDown);
-                const uint32_t dj = 2 * tcount + m;
-                const int dsl = kDown ? (int)(dj % 4) : 0;
-                if (kDown) {
-                    if (!mbar_wait(&b->d_empty[dsl], ((dj / 4) & 1) ^ 1, abort)) { ok = false; break; }
-                } else if (!mbar_wait(&b->d_empty[ds.s0], (use[ds.s0] & 1) ^ 1, abort) ||
-                           (ds.two && !mbar_wait(&b->d_empty[ds.s1], (use[ds.s1] & 1) ^ 1, abort))) {
-                    ok = false;
-                    break;
-                }
+        // MMA issuer m: the whole warp walks the loop, so its counters and descriptors stay
+        // warp-uniform; one elected lane issues every tcgen05.mma and commit
+        const int m = warp - kTmMmaWarp;   // this warp's accumulator D_m and A matrix m
+        const bool leader = elect_one();
+        uint32_t it = 0, tcount = 0, sc = 0, use[3] = {0, 0, 0};
+        bool ok = true;
+        const uint64_t xdesc0 = sw128_desc(smem_u32(xring));   // start address advances 16 B per unit
+        for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x, ++tcount) {
+            const int N = tile_n(p.tiles[tile].z);
+            const bool stacked = kDown && down_stacked(N);   // hi and lo rows as one B operand of 2N rows
+            const uint32_t idesc = idesc_bf16_f32(128, stacked ? 2 * N : N);
+            // gate/up: one or two slots per tile (d_slots); down: use j = 2 tcount + m of the
+            // slot ring, slot j % 4, phase j / 4 (the next tile's two matrices take the two
+            // slots the current tile does not use)
+            const DSlots ds = d_slots(sc, N, kDown);
+            const uint32_t dj = 2 * tcount + m;
+            const int dsl = kDown ? (int)(dj % 4) : 0;
+            if (kDown) {
+                if (!mbar_wait_warp(&b->d_empty[dsl], ((dj / 4) & 1) ^ 1, abort)) { ok = false; break; }
+            } else if (!mbar_wait_warp(&b->d_empty[ds.s0], (use[ds.s0] & 1) ^ 1, abort) ||
+                       (ds.two && !mbar_wait_warp(&b->d_empty[ds.s1], (use[ds.s1] & 1) ^ 1, abort))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t dm = tmem + (kDown ? C::DCOL0 + C::DW * dsl : (m ? ds.col1 : ds.col0));
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int as = it % C::A, xs = it % C::RX;
+                if (!mbar_wait_warp(&b->ready[it % kTmKD], (it / kTmKD) & 1, abort)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t dm = tmem + (kDown ? C::DCOL0 + C::DW * dsl : (m ? ds.col1 : ds.col0));
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int as = it % C::A, xs = it % C::RX;
-                    if (!mbar_wait(&b->ready[it % kTmKD], (it / kTmKD) & 1, abort)) { ok = false; break; }
-                    tc_fence_after();
-                    if (m == 0) TM_TRACE(TT_MW, it);
-                    const uint64_t xd = xdesc0 + (uint64_t)((xs * C::XS) >> 4);
-                    const uint32_t a0 = tmem + 64u * as + 32u * m;
-                    // both loops fully unrolled: the issuing thread's instruction count sets its pace
+                if (m == 0 && leader) TM_TRACE(TT_MW, it);
+                const uint64_t xd = xdesc0 + (uint64_t)((xs * C::XS) >> 4);
+                const uint32_t a0 = tmem + 64u * as + 32u * m;
+                // both loops fully unrolled: the issuing thread's instruction count sets its pace
+                if (leader) {
                     if (C::PARTS == 1 || stacked) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
@@ -388,29 +391,38 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                         for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
                             for (int part = 0; part < C::PARTS; ++part)
-                                tc_mma_bf16_ts(dm, a0 + 8u * ks, xd + (uint64_t)((part * C::XPART + ks * 32) >> 4), idesc,
-                                               (kb | ks | part) ? 1u : 0u);
+                                tc_mma_bf16_ts(dm, a0 + 8u * ks, xd + (uint64_t)((part * C::XPART + ks * 32) >> 4),
+                                               idesc, (kb | ks | part) ? 1u : 0u);
                         }
                     }
                     tc_commit(&b->kb_done[it % kTmKD]);
                     if (m == 0) TM_TRACE(TT_MD, it);
                 }
-                if (!ok) break;
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (leader) {
                 if (kDown) {
                     tc_commit(&b->d_full[dsl]);
                 } else {
                     tc_commit(&b->d_full[ds.s0]);
                     if (ds.two) tc_commit(&b->d_full[ds.s1]);
-                    use[ds.s0]++;
-                    if (ds.two) use[ds.s1]++;
-                    sc += ds.two ? 2 : 1;
                 }
             }
+            __syncwarp();
+            if (!kDown) {
+                use[ds.s0]++;
+                if (ds.two) use[ds.s1]++;
+                sc += ds.two ? 2 : 1;
+            }
+        }
+        if (leader) {
             if (!ok) tm_abort(abort, p.status);
             tc_commit(&b->drain[m]);
-            int never = 0;
-            mbar_wait(&b->drain[m], 0, &never);
         }
+        __syncwarp();
+        int never = 0;
+        mbar_wait(&b->drain[m], 0, &never);
     } else if (warp < kTmDeqWarps) {
         // dequant: set (warp >> 3) takes the K blocks of its parity; thread -> row r of matrix m
         const int set = warp >> 3, m = (warp >> 2) & 1, q = warp & 3, r = 32 * q + lane;

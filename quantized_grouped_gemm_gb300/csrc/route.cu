@@ -92,6 +92,8 @@ constexpr int kRtStages = 4;
 constexpr int kRtA = 128 * 128;   // 128 tokens x 64 bf16
 constexpr int kRtB = 256 * 128;   // 256 experts x 64 bf16
 constexpr int kRtSmem = kRtStages * (kRtA + kRtB) + 256 + 1024;
+constexpr int kRtRowStride = 1040;   // epilogue staging: 128 rows of 1 KB partial logits, padded
+static_assert(128 * kRtRowStride <= kRtStages * (kRtA + kRtB), "router_tc epilogue staging");
 
 __global__ void __launch_bounds__(192, 1)
     router_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, RouteArgs a,
@@ -181,23 +183,34 @@ __global__ void __launch_bounds__(192, 1)
             tc_commit(tmfull);     // also drains every MMA before the epilogue / dealloc
         }
     } else {
-        const int q = warp & 3;
+        // epilogue: thread -> token row 32 q + lane.  Its 256 partial logits go from TMEM into a
+        // padded row of shared memory (the operand stages, free once every MMA has completed;
+        // the 1040-byte row stride keeps the 16-byte stores of 8 consecutive threads on distinct
+        // banks), then out as one 1 KB bulk copy per row.
+        const int q = warp & 3, rl = 32 * q + lane;
         const bool got = mbar_wait(tmfull, 0, abort);
         if (__all_sync(0xffffffffu, got)) {
             tc_fence_after();
-            const int t = blockIdx.x * 128 + 32 * q + lane;
-            float* dst = reinterpret_cast<float*>(a.ws + a.L.rpart) + ((size_t)blockIdx.y * a.T + t) * 256;
+            const int t = blockIdx.x * 128 + rl;
+            float* srow = reinterpret_cast<float*>(smem + (size_t)rl * kRtRowStride);
             for (int c = 0; c < 16; ++c) {
                 uint32_t v[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * c, v);
                 tmem_ld_wait();
-                if (t < a.T) {
-                    float4* d4 = reinterpret_cast<float4*>(dst + 16 * c);
+                float4* d4 = reinterpret_cast<float4*>(srow + 16 * c);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        d4[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                            __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
-                }
+                for (int u = 0; u < 4; ++u)
+                    d4[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                        __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+            }
+            if (t < a.T) {
+                fence_proxy_async_smem();
+                float* dst = reinterpret_cast<float*>(a.ws + a.L.rpart) + ((size_t)blockIdx.y * a.T + t) * 256;
+                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], 1024;" ::"l"(dst),
+                             "r"(smem_u32(srow))
+                             : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // before the CTA's smem goes
             }
         }
         tc_fence_before();
