@@ -14,7 +14,7 @@
 //   route_certify_topk per token: an error bound picks the candidates that can be in the top-8
 //                      of the fixed-order logits; only those are recomputed exactly (CUDA
 //                      cores, fixed fp32 order) and ranked; weights; per-block counts.
-//   route_scan         one CTA: per-block bases, counts, offsets, the exported block map
+//   route_scan         8 CTAs: per-block bases, counts, offsets, the exported block map
 //                      and the GEMM tile lists (expert, first row, rows, weight tile).
 //   route_scatter      one CTA per (block, slot): stable group positions (rank of the token among
 //                      the block's tokens routed to the same expert, from a bitmask), perm /
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
         __syncwarp();
     }
     __syncthreads();
-    // per 32-token block counts (cleared by the scan)
+    // per 32-token block counts (cleared by route_scatter once route_scan has read them)
     int32_t* blk_counts = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
     const size_t blk = (size_t)blockIdx.x * kCertTokens / kRouteBlockTokens;
     for (int i = threadIdx.x; i < 256; i += blockDim.x)
@@ -507,9 +507,13 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
 }
 
 // ---------------------------------------------------------------------------------------
-// route_scan: one CTA of 1024 threads.  Thread (e, part) sums the counts of expert e over a
-// quarter of the token blocks; then per-block bases, counts, offsets (exclusive scan over
-// experts), the exported block map and the GEMM tile lists.
+// route_scan: kScanCtas CTAs of 1024 threads.  In every CTA thread (e, part) sums the counts of
+// expert e over a quarter of the token blocks, and the CTA computes the counts, offsets
+// (exclusive scan over experts) and the per-expert tile scans; the writes are shared out: CTA c
+// writes the per-block bases of experts [32c, 32c + 32) (kScanCtas = 8) and its contiguous
+// share of the exported block map and of each GEMM tile list; CTA 0 writes counts, offsets and
+// the list lengths.  (The per-block counts are cleared by route_scatter, which runs after every
+// CTA here has read them.)
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ int block_exclusive_scan256(int v, int* s_tmp) {
     // called by the 256 threads of warps 0..7 only; s_tmp has 8 ints; uses named barrier 1
@@ -541,17 +545,17 @@ __device__ __forceinline__ int scan_owner(const int* sc, int t) {
     return lo;
 }
 
-// All n entries of a GEMM tile list, written by the CTA's threads: position j holds the shared
+// Entries j0 <= j < j1 of a GEMM tile list, written by the CTA's threads: position j holds the shared
 // expert's entry j - from when from <= j < from + nsh * mt, else routed entry jj (jj = j before
 // the shared block, j - nsh * mt after it) = (token block jj / mt, weight tile jj % mt) of the
 // routed experts' blocks in expert order (sb: exclusive scan of their block counts).  An
 // expert's cnt rows from off are cut into nb near-equal blocks: block i has q + (i < r) rows
 // (q = cnt / nb, r = cnt % nb) and starts at off + i q + min(i, r); the shared expert cuts the
 // T token rows the same way into nsh blocks.  Entry = (expert, first row, rows, weight tile).
-__device__ void gemm_list_entries(int4* list, int n, int mt, int nsh, int from, const int* sb, const int* cnt,
-                                  const int* off, int T, int E) {
+__device__ void gemm_list_entries(int4* list, int j0, int j1, int mt, int nsh, int from, const int* sb,
+                                  const int* cnt, const int* off, int T, int E) {
     const int nsh_e = nsh * mt;
-    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
         int ex, i, m, rows, nb, r0;
         if (j >= from && j < from + nsh_e) {
             const int q = j - from;
@@ -569,6 +573,7 @@ __device__ void gemm_list_entries(int4* list, int n, int mt, int nsh, int from, 
     }
 }
 
+constexpr int kScanCtas = 8;
 __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     __shared__ int s_tmp[8];
     __shared__ int s_part[4][256];
@@ -577,8 +582,9 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     __shared__ int s_tb[257], s_gb[257], s_db[257];   // exclusive scans: block-map tiles, GEMM blocks
     pdl_wait();
     pdl_launch_dependents();
-    const int E = 256;
+    const int E = 256, cta = blockIdx.x, S = gridDim.x;
     const int e = threadIdx.x & 255, part = threadIdx.x >> 8;
+    const bool own_e = (e * S) / E == cta;   // this CTA writes the per-block bases of expert e
     int32_t* blk_counts = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
     int32_t* blk_base = blk_counts + (size_t)a.L.nblk * E;
     const int nb = a.L.nblk, nq = (nb + 3) / 4;
@@ -613,26 +619,24 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
         run += s_part[q][e];
     }
     if (part == 0) {
-        a.counts[e] = run;
         const int off = block_exclusive_scan256(run, s_tmp);
         s_off[e] = off;
-        a.offsets[e] = off;
-        if (e == E - 1) a.offsets[E] = off + run;
+        if (cta == 0) {
+            a.counts[e] = run;
+            a.offsets[e] = off;
+            if (e == E - 1) a.offsets[E] = off + run;
+        }
     }
     __syncthreads();
-    // per-block bases: offsets[e] + counts of e in earlier blocks; the counts are cleared (the
-    // next call adds into zeros)
-    if (in_regs) {
+    // per-block bases: offsets[e] + counts of e in earlier blocks
+    if (own_e && in_regs) {
         int r = s_off[e] + pre;
 #pragma unroll
         for (int u = 0; u < kScanRegs; ++u) {
-            if (b0 + u < b1) {
-                blk_base[(size_t)(b0 + u) * E + e] = r;
-                blk_counts[(size_t)(b0 + u) * E + e] = 0;
-            }
+            if (b0 + u < b1) blk_base[(size_t)(b0 + u) * E + e] = r;
             r += creg[u];
         }
-    } else {
+    } else if (own_e) {
         int r = s_off[e] + pre;
         int b = b0;
         for (; b + 8 <= b1; b += 8) {
@@ -643,14 +647,11 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
             for (int u = 0; u < 8; ++u) {
                 blk_base[(size_t)(b + u) * E + e] = r;
                 r += c[u];
-                blk_counts[(size_t)(b + u) * E + e] = 0;
             }
         }
         for (; b < b1; ++b) {
-            const int c = blk_counts[(size_t)b * E + e];
             blk_base[(size_t)b * E + e] = r;
-            r += c;
-            blk_counts[(size_t)b * E + e] = 0;
+            r += blk_counts[(size_t)b * E + e];
         }
     }
     // per expert: tiles of the exported block map and token blocks of the two GEMM tile lists,
@@ -679,7 +680,8 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     // Exported block map: ceil(count / tile_rows) tiles per expert, expert-ascending.
     const int BM = a.tile_rows;
     const int ntile = s_tb[E];
-    for (int t = threadIdx.x; t < ntile; t += blockDim.x) {
+    for (int t = (int)((long long)ntile * cta / S) + threadIdx.x; t < (int)((long long)ntile * (cta + 1) / S);
+         t += blockDim.x) {
         const int ex = scan_owner(s_tb, t), i = t - s_tb[ex];
         int32_t* tt = a.tiles + 3 * (size_t)t;
         tt[0] = ex;
@@ -699,9 +701,11 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
     const int ngu = (nsh + s_gb[E]) * MTgu, ndn = (nshd + s_db[E]) * MTdn;
     const int pg = shared_tiles_at(ngu, nsh * MTgu, a.num_sms);
     const int pd = shared_tiles_at(ndn, nshd * MTdn, a.num_sms);
-    gemm_list_entries(reinterpret_cast<int4*>(a.ws + a.L.gu_tiles), ngu, MTgu, nsh, pg, s_gb, s_cnt, s_off, a.T, E);
-    gemm_list_entries(reinterpret_cast<int4*>(a.ws + a.L.dn_tiles), ndn, MTdn, nshd, pd, s_db, s_cnt, s_off, a.T, E);
-    if (threadIdx.x == 0) {
+    gemm_list_entries(reinterpret_cast<int4*>(a.ws + a.L.gu_tiles), (int)((long long)ngu * cta / S),
+                      (int)((long long)ngu * (cta + 1) / S), MTgu, nsh, pg, s_gb, s_cnt, s_off, a.T, E);
+    gemm_list_entries(reinterpret_cast<int4*>(a.ws + a.L.dn_tiles), (int)((long long)ndn * cta / S),
+                      (int)((long long)ndn * (cta + 1) / S), MTdn, nshd, pd, s_db, s_cnt, s_off, a.T, E);
+    if (cta == 0 && threadIdx.x == 0) {
         *a.num_tiles = ntile;
         *reinterpret_cast<int32_t*>(a.ws + a.L.gu_num) = ngu;
         *reinterpret_cast<int32_t*>(a.ws + a.L.dn_num) = ndn;
@@ -712,8 +716,8 @@ __global__ void __launch_bounds__(1024) route_scan(RouteArgs a) {
 // route_scatter: grid = (ceil(T/32) blocks, k slots), 256 threads.  Every CTA rebuilds the
 // block's expert bitmasks (bit t set when token t of the block picked the expert), which
 // give the stable rank of a token among the block's tokens routed to the same expert; CTA
-// (b, j) then writes pos / perm of slot j, copies those 32 rows into expert order
-// (xs[p] = x[t]) and clears 1/k of the block's rows of the fp32 token-order sum.
+// (b, j) then writes pos / perm of slot j and copies those 32 rows into expert order
+// (xs[p] = x[t]); CTA (b, 0) also clears the block's per-expert counts for the next call.
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) route_scatter(RouteArgs a) {
     __shared__ uint32_t s_mask[256];
@@ -726,6 +730,8 @@ __global__ void __launch_bounds__(256) route_scatter(RouteArgs a) {
     pdl_wait();
     pdl_launch_dependents();
     s_mask[threadIdx.x] = 0;
+    // the block's per-expert counts have been read by route_scan: clear them for the next call
+    if (slot == 0) reinterpret_cast<int32_t*>(a.ws + a.L.blk)[(size_t)blockIdx.x * E + threadIdx.x] = 0;
     __syncthreads();
     const int tl = threadIdx.x / 8, j = threadIdx.x % 8;   // k == 8
     int e = -1;
@@ -924,7 +930,7 @@ cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned l
     if ((err = launch_with_pdl(route_certify_topk, dim3((a.T + kCertTokens - 1) / kCertTokens), dim3(32 * kCertTokens),
                                0, st, a, KS)) != cudaSuccess)
         return err;
-    if ((err = launch_with_pdl(route_scan, dim3(1), dim3(1024), 0, st, a)) != cudaSuccess) return err;
+    if ((err = launch_with_pdl(route_scan, dim3(kScanCtas), dim3(1024), 0, st, a)) != cudaSuccess) return err;
     return launch_with_pdl(route_scatter, dim3(nblk, a.k), dim3(256), 0, st, a);
 }
 
