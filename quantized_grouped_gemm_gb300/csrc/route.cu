@@ -272,20 +272,19 @@ __device__ __forceinline__ void warp_pinned_logits(const uint4 (&xv)[8], const u
     for (int g = 0; g < G; ++g) l[g] = p[g];
 }
 
-template <int G>
+// Exact logits of G experts for one token: NI = d / 256 column groups with the token row in
+// registers (NI <= 8), or NI = 0 for any other d (rows read from memory, one logit at a time).
+template <int NI, int G>
 __device__ __forceinline__ void pinned_logit_group(const uint4 (&xv)[8], const uint16_t* xrow, const uint16_t* w_router,
                                                    int d, const int (&e)[G], int lane, float (&l)[G]) {
     const uint16_t* w[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) w[g] = w_router + (size_t)e[g] * d;
-    switch (d / 256) {
-        case 1: warp_pinned_logits<1, G>(xv, w, lane, l); return;
-        case 2: warp_pinned_logits<2, G>(xv, w, lane, l); return;
-        case 4: warp_pinned_logits<4, G>(xv, w, lane, l); return;
-        case 8: warp_pinned_logits<8, G>(xv, w, lane, l); return;
-        default:
+    if constexpr (NI > 0) {
+        warp_pinned_logits<NI, G>(xv, w, lane, l);
+    } else {
 #pragma unroll
-            for (int g = 0; g < G; ++g) l[g] = warp_pinned_logit(xrow, w[g], d, lane, nullptr);
+        for (int g = 0; g < G; ++g) l[g] = warp_pinned_logit(xrow, w[g], d, lane, nullptr);
     }
 }
 
@@ -340,7 +339,8 @@ static_assert(kRouteBlockTokens % kCertTokens == 0, "certify tokens per CTA");
 constexpr int kCertGroup = MOE_CERT_GROUP;   // exact logits per round
 static_assert(kCertGroup >= 1 && 256 % kCertGroup == 0, "certify group");
 
-__global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs a, int KS) {
+template <int NI>
+__global__ void __launch_bounds__(32 * kCertTokens, 2) route_certify_topk(RouteArgs a, int KS) {
     __shared__ uint32_t s_mask[256];
     __shared__ float s_all[kCertTokens][256];
     __shared__ int s_cand[kCertTokens][32];
@@ -409,21 +409,32 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
             key[s] = logit_key32(lt[s]);
         }
         dmax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(dmax)));   // dmax >= 0
-        // the 8th largest l~: eight rounds, each removing one holder of the largest key
+        // the 8th largest l~ (with multiplicity): each lane sorts its eight keys (descending,
+        // Batcher's odd-even merge network), then eight rounds each remove the head of the lowest
+        // lane holding the largest head
+        {
+            auto cx = [&](int i, int j) {   // key[i] >= key[j] afterwards
+                const uint32_t hi = max(key[i], key[j]), lo = min(key[i], key[j]);
+                key[i] = hi;
+                key[j] = lo;
+            };
+            cx(0, 1); cx(2, 3); cx(4, 5); cx(6, 7);
+            cx(0, 2); cx(1, 3); cx(4, 6); cx(5, 7);
+            cx(1, 2); cx(5, 6);
+            cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
+            cx(2, 4); cx(3, 5);
+            cx(1, 2); cx(3, 4); cx(5, 6);
+        }
         uint32_t top = 0;
+#pragma unroll
         for (int j = 0; j < 8; ++j) {
-            uint32_t mx = key[0];
+            top = __reduce_max_sync(0xffffffffu, key[0]);
+            const uint32_t holders = __ballot_sync(0xffffffffu, key[0] == top);
+            if (lane == __ffs(holders) - 1) {
 #pragma unroll
-            for (int s = 1; s < 8; ++s) mx = max(mx, key[s]);
-            top = __reduce_max_sync(0xffffffffu, mx);
-            int mine = 0x7fffffff;
-#pragma unroll
-            for (int s = 7; s >= 0; --s)
-                if (key[s] == top) mine = 8 * lane + s;
-            const int who = __reduce_min_sync(0xffffffffu, mine);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                if (8 * lane + s == who) key[s] = 0u;
+                for (int s = 0; s < 7; ++s) key[s] = key[s + 1];
+                key[7] = 0u;
+            }
         }
         const float lo = __fsub_rd(key32_logit(top), dmax);
         uint32_t cm[8];
@@ -447,18 +458,26 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
             __syncwarp();
             int my_e = -1;
             float my_l = -INFINITY;
-            for (int j0 = 0; j0 < ncand; j0 += kCertGroup) {
-                int eg[kCertGroup];
+            // rounds of kCertGroup candidates, then the remaining one to three in rounds of 2 and 1
+            // (every load of a round is in flight at once)
+            auto round = [&](auto gsz, int j0) {
+                constexpr int G = decltype(gsz)::value;
+                int eg[G];
 #pragma unroll
-                for (int g = 0; g < kCertGroup; ++g) eg[g] = s_cand[warp][min(j0 + g, ncand - 1)];
-                float lg[kCertGroup];
-                pinned_logit_group<kCertGroup>(xv, xrow, a.w_router, a.d, eg, lane, lg);
+                for (int g = 0; g < G; ++g) eg[g] = s_cand[warp][j0 + g];
+                float lg[G];
+                pinned_logit_group<NI, G>(xv, xrow, a.w_router, a.d, eg, lane, lg);
 #pragma unroll
-                for (int g = 0; g < kCertGroup; ++g) {
-                    const float v = a.bias ? lg[g] + a.bias[eg[g]] : lg[g];
-                    if (lane == j0 + g && j0 + g < ncand) { my_e = eg[g]; my_l = v; }
-                }
+                for (int g = 0; g < G; ++g)
+                    if (lane == j0 + g) { my_e = eg[g]; my_l = a.bias ? lg[g] + a.bias[eg[g]] : lg[g]; }
+            };
+            int j0 = 0;
+            for (; j0 + kCertGroup <= ncand; j0 += kCertGroup) round(std::integral_constant<int, kCertGroup>{}, j0);
+            if (ncand - j0 >= 2) {
+                round(std::integral_constant<int, 2>{}, j0);
+                j0 += 2;
             }
+            if (ncand - j0 == 1) round(std::integral_constant<int, 1>{}, j0);
             // top-k among the exact candidate logits, one per lane
             uint32_t k1 = my_e >= 0 ? logit_key32(my_l) : 0u;
             int sel_e = -1;
@@ -483,7 +502,7 @@ __global__ void __launch_bounds__(32 * kCertTokens) route_certify_topk(RouteArgs
 #pragma unroll
                 for (int g = 0; g < kCertGroup; ++g) eg[g] = e0 + g;
                 float lg[kCertGroup];
-                pinned_logit_group<kCertGroup>(xv, xrow, a.w_router, a.d, eg, lane, lg);
+                pinned_logit_group<NI, kCertGroup>(xv, xrow, a.w_router, a.d, eg, lane, lg);
 #pragma unroll
                 for (int g = 0; g < kCertGroup; ++g)
                     if (lane == ((e0 + g) & 31)) s_all[warp][e0 + g] = a.bias ? lg[g] + a.bias[e0 + g] : lg[g];
@@ -908,6 +927,19 @@ __global__ void __launch_bounds__(128) route_decode(RouteArgs a) {
 
 }  // namespace
 
+// route_certify_topk instantiated for the token row in registers (d = 256, 512, 1024, 2048) or
+// read from memory (other d)
+static cudaError_t launch_certify(const RouteArgs& a, int KS, cudaStream_t st) {
+    const dim3 grid((a.T + kCertTokens - 1) / kCertTokens), block(32 * kCertTokens);
+    switch (a.d / 256) {
+        case 1: return launch_with_pdl(route_certify_topk<1>, grid, block, 0, st, a, KS);
+        case 2: return launch_with_pdl(route_certify_topk<2>, grid, block, 0, st, a, KS);
+        case 4: return launch_with_pdl(route_certify_topk<4>, grid, block, 0, st, a, KS);
+        case 8: return launch_with_pdl(route_certify_topk<8>, grid, block, 0, st, a, KS);
+        default: return launch_with_pdl(route_certify_topk<0>, grid, block, 0, st, a, KS);
+    }
+}
+
 cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned long long* launches) {
     static bool attr = false;
     if (!attr) {
@@ -927,9 +959,7 @@ cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned l
     if ((err = launch_with_pdl(router_tc, dim3((a.T + 127) / 128, KS), dim3(192), kRtSmem, st, tm_x, tm_w, a, KS)) !=
         cudaSuccess)
         return err;
-    if ((err = launch_with_pdl(route_certify_topk, dim3((a.T + kCertTokens - 1) / kCertTokens), dim3(32 * kCertTokens),
-                               0, st, a, KS)) != cudaSuccess)
-        return err;
+    if ((err = launch_certify(a, KS, st)) != cudaSuccess) return err;
     if ((err = launch_with_pdl(route_scan, dim3(kScanCtas), dim3(1024), 0, st, a)) != cudaSuccess) return err;
     return launch_with_pdl(route_scatter, dim3(nblk, a.k), dim3(256), 0, st, a);
 }
@@ -937,8 +967,10 @@ cudaError_t launch_route_prefill(const RouteArgs& a, cudaStream_t st, unsigned l
 namespace {
 // ---------------------------------------------------------------------------------------
 // router_logits_exact: every logit of every token with the exact recomputation's device code
-// (pinned_logit_group, kCertGroup experts per round); one warp per (token, 32 experts).
+// (pinned_logit_group, kCertGroup experts per round; NI = d / 256 as in route_certify_topk);
+// one warp per (token, 32 experts).
 // ---------------------------------------------------------------------------------------
+template <int NI>
 __global__ void __launch_bounds__(256) router_logits_exact(const uint16_t* __restrict__ x,
                                                            const uint16_t* __restrict__ w_router,
                                                            const float* __restrict__ bias, float* __restrict__ out,
@@ -961,7 +993,7 @@ __global__ void __launch_bounds__(256) router_logits_exact(const uint16_t* __res
 #pragma unroll
         for (int g = 0; g < kCertGroup; ++g) eg[g] = e0 + g0 + g;
         float lg[kCertGroup];
-        pinned_logit_group<kCertGroup>(xv, xrow, w_router, d, eg, lane, lg);
+        pinned_logit_group<NI, kCertGroup>(xv, xrow, w_router, d, eg, lane, lg);
 #pragma unroll
         for (int g = 0; g < kCertGroup; ++g)
             if (lane == g0 + g) out[(size_t)t * 256 + eg[g]] = bias ? lg[g] + bias[eg[g]] : lg[g];
@@ -972,7 +1004,14 @@ __global__ void __launch_bounds__(256) router_logits_exact(const uint16_t* __res
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w_router, const float* bias, float* out, int T,
                                  int d, cudaStream_t st, unsigned long long* launches) {
     *launches += 1;
-    return launch_with_pdl(router_logits_exact, dim3((unsigned)T), dim3(256), 0, st, x, w_router, bias, out, T, d);
+    const dim3 grid((unsigned)T), block(256);
+    switch (d / 256) {
+        case 1: return launch_with_pdl(router_logits_exact<1>, grid, block, 0, st, x, w_router, bias, out, T, d);
+        case 2: return launch_with_pdl(router_logits_exact<2>, grid, block, 0, st, x, w_router, bias, out, T, d);
+        case 4: return launch_with_pdl(router_logits_exact<4>, grid, block, 0, st, x, w_router, bias, out, T, d);
+        case 8: return launch_with_pdl(router_logits_exact<8>, grid, block, 0, st, x, w_router, bias, out, T, d);
+        default: return launch_with_pdl(router_logits_exact<0>, grid, block, 0, st, x, w_router, bias, out, T, d);
+    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -1079,9 +1118,7 @@ cudaError_t launch_route_prefill_host(const RouteArgs& a, cudaStream_t st, unsig
     if ((err = launch_with_pdl(router_tc, dim3((a.T + 127) / 128, KS), dim3(192), kRtSmem, st, tm_x, tm_w, a, KS)) !=
         cudaSuccess)
         return err;
-    if ((err = launch_with_pdl(route_certify_topk, dim3((a.T + kCertTokens - 1) / kCertTokens), dim3(32 * kCertTokens),
-                               0, st, a, KS)) != cudaSuccess)
-        return err;
+    if ((err = launch_certify(a, KS, st)) != cudaSuccess) return err;
     // the round trip: per-block counts to the host, scan and block map there, results back
     int32_t* blk_dev = reinterpret_cast<int32_t*>(a.ws + a.L.blk);
     std::vector<int32_t> blk((size_t)nblk * E);
