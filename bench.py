@@ -151,15 +151,14 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------- work
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a workload's
-# dominant kernel, from an ncu full capture of the current kernels (profiles/ncu_*.md):
-# {workload: (kernel, bytes)}.  A workload whose dominant kernel differs, or is not listed,
-# reports null.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each of a
+# workload's kernels, from an ncu full capture of the current kernels (profiles/ncu_*.md):
+# {workload: {kernel: bytes}}.  A kernel that is not listed reports null.
 TRAFFIC_BYTES = {
-    "skew_t16384_d2048": ("down", 122.412032e6 + 3.427584e6),
-    "prefill_t4096_d2048": ("gate_up", 454.353408e6 + 62.073344e6),
-    "prefill_t512_d2048": ("gate_up", 322.279936e6 + 10.222336e6),
-    "decode_t1_d2048": ("decode", 17.078528e6),
+    "skew_t16384_d2048": {"gate_up": 177.041664e6 + 48.105728e6, "down": 122.410752e6 + 3.551488e6},
+    "prefill_t4096_d2048": {"gate_up": 454.321408e6 + 62.455552e6, "down": 276.634880e6 + 27.969536e6},
+    "prefill_t512_d2048": {"gate_up": 322.278400e6 + 10.638336e6, "down": 165.398272e6 + 4.000512e6},
+    "decode_t1_d2048": {"decode": 17.078528e6},
 }
 
 
@@ -389,7 +388,7 @@ def run_ours(wname, args, rank, world, local, headline=True):
     P = peaks()
     res = dict(metric=METRIC, n_gpus=world, steps=K, warmup=warmup_steps, ms_per_step=ms_step, data="synthetic",
                scaling="weak", vs_baseline=None, dtype="bf16", clocks=clk, gpu_launches=int(launches_per_step * K))
-    traffic = TRAFFIC_BYTES.get(wl.name)
+    traffic = TRAFFIC_BYTES.get(wl.name, {})
     if decode:
         us_tok_layer = ms_step * 1000.0 / layers
         res.update(value=us_tok_layer, unit="us/token/layer", higher_is_better=False)
@@ -397,7 +396,7 @@ def run_ours(wname, args, rank, world, local, headline=True):
         bytes_layer = sh.E * sh.d * 2 + 9 * (3 * sh.d * sh.I // 2 + 3 * sh.d * sh.I // 64 * 4)
         res["roofline"] = roofline_entry("decode_fused (one launch per layer: route + gate/up + down + combine)", P,
                                          bytes_layer, us_tok_layer * 1e-3, "hbm", long_region,
-                                         traffic[1] if traffic else None)
+                                         traffic.get("decode"))
         res["roofline"]["bytes_per_token_layer"] = bytes_layer
         res["config"] = dict(workload=wl.name, T=1, d=sh.d, E=sh.E, k=sh.k, I=sh.I, I_shared=sh.I_shared,
                              layers=layers, l2=f"inputs larger than L2: {layers} layer copies of the weights, "
@@ -417,7 +416,7 @@ def run_ours(wname, args, rank, world, local, headline=True):
                 if down_dom else "ffn_tm_kernel<0,0> (gate/up + SwiGLU; tcgen05, dequantised weights in TMEM)")
         flops, byts, kms = (A["dn_flops"], A["dn_bytes"], dn_ms) if down_dom else (A["gu_flops"], A["gu_bytes"], gu_ms)
         hbm = flops / byts < ridge
-        tr = traffic[1] if traffic and traffic[0] == ("down" if down_dom else "gate_up") else None
+        tr = traffic.get("down" if down_dom else "gate_up")
         res["roofline"] = roofline_entry(name, P, byts if hbm else flops, kms, "hbm" if hbm else "tensor",
                                          long_region, tr)
         ffn_ms = gu_ms + dn_ms
