@@ -283,52 +283,59 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     }
 
     if (warp == kTmCodeWarp) {
-        // packed codes of every (tile, K block), up to RC K blocks ahead of the dequant
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
-                const int4 t = p.tiles[tile];
-                const uint8_t* w = t.x < p.E ? p.w_routed + (size_t)(t.x * WT + t.w) * KB * C::CH
-                                             : p.w_shared + (size_t)t.w * KB * C::CH;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int cs = it % C::RC;
-                    if (!mbar_wait(&b->c_empty[cs], ((it / C::RC) & 1) ^ 1, abort)) { ok = false; break; }
+        // packed codes of every (tile, K block), up to RC K blocks ahead of the dequant; the whole
+        // warp walks the loop (warp-uniform counters and addresses), one elected lane issues
+        const bool leader = elect_one();
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
+            const int4 t = p.tiles[tile];
+            const uint8_t* w = t.x < p.E ? p.w_routed + (size_t)(t.x * WT + t.w) * KB * C::CH
+                                         : p.w_shared + (size_t)t.w * KB * C::CH;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int cs = it % C::RC;
+                if (!mbar_wait_warp(&b->c_empty[cs], ((it / C::RC) & 1) ^ 1, abort)) { ok = false; break; }
+                if (leader) {
                     mbar_arrive_expect_tx(&b->c_full[cs], C::CH);
-                    bulk_g2s(cring + cs * C::CH, w + (size_t)kb * C::CH, C::CH,
-                             &b->c_full[cs]);
+                    bulk_g2s(cring + cs * C::CH, w + (size_t)kb * C::CH, C::CH, &b->c_full[cs]);
                     TM_TRACE(TT_PC, it);
                 }
+                __syncwarp();
             }
+        }
+        if (leader) {
             if (!ok) tm_abort(abort, p.status);
             tm_drain(b->c_full, C::RC, C::RC, it);
         }
+        __syncwarp();
     } else if (warp == kTmXWarp) {
         // token rows of every (tile, K block), up to RX K blocks ahead of the MMA; for the down
-        // projection the lo half of h follows the hi rows directly when the tile stacks (N <= 32)
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
-                const int4 t = p.tiles[tile];
-                const int e = t.x, row0 = t.y, N = tile_n(t.z);
-                const int xrow0 = kDown ? (e < p.E ? row0 : p.k * p.T + row0) : row0;
-                const CUtensorMap* tms = (kDown || e < p.E) ? &tm_a : &tm_b;
-                const CUtensorMap* tml = (kDown || e < p.E) ? &tm_al : &tm_bl;
-                const int lo_off = down_stacked(N) ? N * 128 : C::XPART;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int xs = it % C::RX;
-                    if (it >= (uint32_t)C::RX) {
-                        const uint32_t g = it - C::RX;
-                        if (!mbar_wait(&b->kb_done[g % kTmKD], (g / kTmKD) & 1, abort)) { ok = false; break; }
-                    }
-                    // (the wait above also means that the ready barrier's phase for K block
-                    // it - 8 has completed: its MMAs were issued)
+        // projection the lo half of h follows the hi rows directly when the tile stacks (N <= 32);
+        // the whole warp walks the loop, one elected lane issues
+        const bool leader = elect_one();
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num && ok; tile += gridDim.x) {
+            const int4 t = p.tiles[tile];
+            const int e = t.x, row0 = t.y, N = tile_n(t.z);
+            const int xrow0 = kDown ? (e < p.E ? row0 : p.k * p.T + row0) : row0;
+            const CUtensorMap* tms = (kDown || e < p.E) ? &tm_a : &tm_b;
+            const CUtensorMap* tml = (kDown || e < p.E) ? &tm_al : &tm_bl;
+            const int lo_off = down_stacked(N) ? N * 128 : C::XPART;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int xs = it % C::RX;
+                if (it >= (uint32_t)C::RX) {
+                    const uint32_t g = it - C::RX;
+                    if (!mbar_wait_warp(&b->kb_done[g % kTmKD], (g / kTmKD) & 1, abort)) { ok = false; break; }
+                }
+                // (the wait above also means that the ready barrier's phase for K block
+                // it - 8 has completed: its MMAs were issued)
 #ifdef MOE_TEST_DROP_TOKEN_BLOCK
-                    // timeout test build only: CTA 0 never arms this K block's ready barrier, so
-                    // the MMA threads' bounded wait on it runs out and the CTA unwinds
-                    if (blockIdx.x == 0 && it == (uint32_t)(MOE_TEST_DROP_TOKEN_BLOCK)) continue;
+                // timeout test build only: CTA 0 never arms this K block's ready barrier, so
+                // the MMA threads' bounded wait on it runs out and the CTA unwinds
+                if (blockIdx.x == 0 && it == (uint32_t)(MOE_TEST_DROP_TOKEN_BLOCK)) continue;
 #endif
+                if (leader) {
                     uint64_t* rdy = &b->ready[it % kTmKD];
                     mbar_arrive_expect_tx(rdy, C::PARTS * N * 128);
                     uint8_t* dst = xring + xs * C::XS;
@@ -342,10 +349,14 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                     }
                     TM_TRACE(TT_PX, it);
                 }
+                __syncwarp();
             }
+        }
+        if (leader) {
             if (!ok) tm_abort(abort, p.status);
             tm_drain(b->ready, kTmKD, C::RX, it);   // the token rows of the last RX blocks have landed
         }
+        __syncwarp();
     } else if (warp >= kTmMmaWarp) {
         // MMA issuer m: the whole warp walks the loop, so its counters and descriptors stay
         // warp-uniform; one elected lane issues every tcgen05.mma and commit
