@@ -134,17 +134,22 @@ __global__ void __launch_bounds__(192, 1)
     }
     pdl_wait();
     pdl_launch_dependents();
+    // producer (warp 0) and MMA issuer (warp 1) walk their loops with the whole warp, so counters
+    // and descriptors stay warp-uniform; one elected lane issues
     if (warp == 0) {
-        if (lane == 0) {
-            prefetch_tmap(&tm_x);
-            uint32_t it = 0;
-            for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                const int st = it % kRtStages;
-                if (!mbar_wait(&empty[st], ((it / kRtStages) & 1) ^ 1, abort)) {
+        const bool leader = elect_one();
+        if (leader) prefetch_tmap(&tm_x);
+        uint32_t it = 0;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const int st = it % kRtStages;
+            if (!mbar_wait_warp(&empty[st], ((it / kRtStages) & 1) ^ 1, abort)) {
+                if (leader) {
                     *abort = 1;
                     set_status(status, MOE_STATUS_TIMEOUT);
-                    break;
                 }
+                break;
+            }
+            if (leader) {
                 uint8_t* dst = smem + st * (kRtA + kRtB);
                 if ((int)it < npre) {   // router-weight tile already requested
                     mbar_arrive_expect_tx(&full[st], kRtA);
@@ -154,23 +159,28 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tma_load_2d(dst, &tm_x, kb * kBK, blockIdx.x * 128, &full[st]);
             }
-            // every issued copy lands before the CTA can exit (including router-weight tiles
-            // requested before the wait for stages the loop did not reach after a timeout)
+            __syncwarp();
+        }
+        // every issued copy lands before the CTA can exit (including router-weight tiles
+        // requested before the wait for stages the loop did not reach after a timeout)
+        if (leader) {
             int never = 0;
             const uint32_t last = it > (uint32_t)npre ? it : (uint32_t)npre;
             const uint32_t first = last > (uint32_t)kRtStages ? last - kRtStages : 0;
             for (uint32_t i = first; i < last; ++i) mbar_wait(&full[i % kRtStages], (i / kRtStages) & 1, &never);
         }
+        __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(128, 256);
-            const uint32_t base = smem_u32(smem);
-            uint32_t it = 0;
-            bool ok = true;
-            for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                const int st = it % kRtStages;
-                if (!mbar_wait(&full[st], (it / kRtStages) & 1, abort)) { ok = false; break; }
-                tc_fence_after();
+        const bool leader = elect_one();
+        const uint32_t idesc = idesc_bf16_f32(128, 256);
+        const uint32_t base = smem_u32(smem);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const int st = it % kRtStages;
+            if (!mbar_wait_warp(&full[st], (it / kRtStages) & 1, abort)) { ok = false; break; }
+            tc_fence_after();
+            if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t sa = base + st * (kRtA + kRtB);
@@ -179,9 +189,13 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_commit(&empty[st]);
             }
+            __syncwarp();
+        }
+        if (leader) {
             if (!ok) { *abort = 1; set_status(status, MOE_STATUS_TIMEOUT); }
             tc_commit(tmfull);     // also drains every MMA before the epilogue / dealloc
         }
+        __syncwarp();
     } else {
         // epilogue: thread -> token row 32 q + lane.  Its 256 partial logits go from TMEM into a
         // padded row of shared memory (the operand stages, free once every MMA has completed;
