@@ -155,9 +155,9 @@ class ClockSampler:
 # workload's kernels, from an ncu full capture of the current kernels (profiles/ncu_*.md):
 # {workload: {kernel: bytes}}.  A kernel that is not listed reports null.
 TRAFFIC_BYTES = {
-    "skew_t16384_d2048": {"gate_up": 177.041664e6 + 48.105728e6, "down": 122.410752e6 + 3.551488e6},
-    "prefill_t4096_d2048": {"gate_up": 454.321408e6 + 62.455552e6, "down": 276.634880e6 + 27.969536e6},
-    "prefill_t512_d2048": {"gate_up": 322.278400e6 + 10.638336e6, "down": 165.398272e6 + 4.000512e6},
+    "skew_t16384_d2048": {"gate_up": 177.104384e6 + 47.760896e6, "down": 122.410752e6 + 3.363584e6},
+    "prefill_t4096_d2048": {"gate_up": 454.290432e6 + 62.292992e6, "down": 276.466176e6 + 27.593728e6},
+    "prefill_t512_d2048": {"gate_up": 322.247936e6 + 10.189056e6, "down": 165.381632e6 + 3.507968e6},
     "decode_t1_d2048": {"decode": 17.078528e6},
 }
 
