@@ -10,7 +10,8 @@
 // traffic": gate/up fused with the gated activation; the output projection fused with the
 // routing score and the shared-expert sum.
 //
-// A tile is (expert, block of <= 128 token rows, weight tile).  Every MMA computes
+// A tile is (expert, block of token rows, weight tile): blocks of at most 128 rows (gate/up)
+// or 96 rows (down).  Every MMA computes
 //     D[m][n] (+)= sum_k W[m][k] X[n][k]     M = 128 weight rows, N = 16 ceil(rows / 16), K = 16
 // with W, bf16, read from tensor memory (TMEM) and X, the block's token rows, read from shared
 // memory (128-byte swizzled, K-major).  Writing the dequantised weights to TMEM keeps them off
@@ -22,11 +23,10 @@
 //   down     two A matrices: output rows 256 wt .. +127 and +128 .. +255; h enters as its hi
 //            half and its lo half: for N <= 32 as one B operand of 2N rows (hi rows, then lo
 //            rows; y = D[n] + D[N + n]), else as two MMAs per K step into the same D; weight * y
-//            (fp32) leaves the chunk in one of two ways, chosen by whether the weighted rows fit
-//            well inside L2: stored into Y [d/128][(k+1)T][128] at the row index of h (the rows
-//            of a 32-token chunk are one contiguous block of a 128-column tile: one TMA bulk
-//            copy; plain stores, no atomics), or added into the fp32 token-order sum with one
-//            512-byte bulk reduce-add per token and matrix.
+//            (fp32) of both matrices is staged per 32-token chunk and leaves in one of two ways:
+//            added into the fp32 token-order sum with one 1 KB bulk reduce-add per token
+//            (default), or, in deterministic mode, stored into Y [d/128][(k+1)T][128] at the
+//            row index of h with bulk copies (plain stores, no atomics).
 // combine_rows sums each token's k routed rows and its shared row of Y in a fixed order.
 // Warp roles (28 warps):
 //   0-15  dequant, two sets of 8 warps taking alternate K blocks: warp w owns row 32 (w & 3) +
@@ -39,23 +39,25 @@
 //   24    codes producer: cp.async.bulk of the 9216-byte packed chunk pair of each K block
 //   25    token-row producer: TMA loads of the block's token rows (64-row boxes, then 16-row
 //         boxes for the rest)
-//   26-27 MMA issuers, one thread each: warp 26 + m issues every MMA into D_m (a warp issues a
-//         tcgen05.mma about every 54 cycles, while the tensor core finishes a 128 x N x 16 MMA
-//         with A in TMEM in N / 2 cycles: two issuers double the rate for small N); warp 26
-//         owns the TMEM allocation
+//   26-27 MMA issuers: warp 26 + m issues every MMA into D_m (two issuers: the tensor core
+//         finishes a 128 x N x 16 MMA with A in TMEM in about N / 2 cycles, so for small N the
+//         issue rate matters); warp 26 owns the TMEM allocation
+// Warps 24-27 walk their loops with all 32 lanes, so counters, descriptors and addresses stay
+// warp-uniform, and one lane chosen by elect.sync issues the copies, TMA loads, MMAs and
+// commits (a single lane in a divergent branch issued about one tcgen05.mma per 50 cycles).
 // TMEM (512 columns): an A ring of slots of 64 columns from column 0 (slot s, matrix m, K step ks
-// at 64 s + 32 m + 8 ks), then accumulator slots of 128 columns.
-//   gate/up  4 A slots, 2 D slots: a tile whose two accumulators fit in 128 columns (N <= 64)
-//            takes one slot, so the next tile's MMAs run while the epilogue drains it; a larger
-//            tile takes both (D_m in its own slot).
-//   down     2 A slots (its MMAs are the slower stage), 3 D slots: matrix m of the t-th tile is use
-//            j = 2t + m of the slot ring (slot j % 3); the epilogue drains matrix 0 and frees its
-//            slot before matrix 1, so a matrix's next slot is free before its MMAs need it.
-// MMA threads and epilogue walk the same slot sequence.
-// Each MMA thread commits once per K block to a ring of "K block done" barriers (two arrivals);
+// at 64 s + 32 m + 8 ks), then the accumulator slots.
+//   gate/up  4 A slots, 2 D slots of 128 columns: a tile whose two accumulators fit in 128
+//            columns (N <= 64) takes one slot, so the next tile's MMAs run while the epilogue
+//            drains it; a larger tile takes both (D_m in its own slot).
+//   down     2 A slots, 4 D slots of 96 columns, one matrix each: matrix m of the t-th tile is
+//            use j = 2t + m of the slot ring (slot j % 4), so the next tile's two matrices use
+//            the two slots the current tile does not.
+// MMA issuers and epilogue walk the same slot sequence.
+// Each MMA issuer commits once per K block to a ring of "K block done" barriers (two arrivals);
 // the dequant sets (A slot reuse) and the token-row producer (token-row slot reuse) wait on it.
 // One "ready" barrier per K block collects the dequant set's warps and the token-row bytes, so
-// an MMA thread waits once per K block: the issuing threads set the pace.
+// an MMA issuer waits once per K block.
 // All waits are bounded (MOE_STATUS_TIMEOUT, then the CTA unwinds).
 #include "moe_internal.cuh"
 
