@@ -140,9 +140,9 @@ typedef struct moe_options {
     int gemm_rows;          /* prefill: largest number of token rows in one grouped-GEMM block, 16, 32,
                                64 or 128 (default 128; 0 takes the default, other values are an
                                argument error).  Each expert's rows are cut into near-equal blocks
-                               of at most this many rows, and every block streams its expert's
-                               weights once per projection ("Match tile size to expert load" on the
-                               page).  Used by moe_route, which writes the GEMM tile lists that
+                               of at most this many rows (the down projection caps its blocks at
+                               96 rows), and every block streams its expert's weights once per
+                               projection ("Match tile size to expert load" on the page).  Used by moe_route, which writes the GEMM tile lists that
                                moe_grouped_ffn reads.  Every value gives the same routing and the
                                same outputs up to fp32 summation order.  Ignored by the decode
                                path. */
