@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kFzThreads, 2) decode_fused(FzParams P) {
         __syncwarp();
         __syncthreads();
         if (r2 == 0) FZ_STAMP(9);
-        const int nt = my_dt - 2 * r2 < 2 ? my_dt - 2 * r2 : 2;   // tiles this round
+        const int nt = my_dt - 2 * r2 < 2 ? my_dt - 2 * r2 : 2;   // tiles this pass
         // weight * partial rows go into the fp32 sum (order of the additions not fixed)
         for (int u2 = 0; u2 < nt; ++u2) {
             const int dt = c + kFzCluster * (2 * r2 + u2);
@@ -624,13 +624,13 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t st, unsig
 
     // Can every cluster be resident at once with `smem` bytes per CTA (the grid waits on
     // itself)?  Checked once per (device, size, units).
-    auto fits = [&](size_t smem, int& verdict) -> cudaError_t {
+    auto fits = [&](size_t smem, int& fit_ok) -> cudaError_t {
         std::lock_guard<std::mutex> lock(g_fz_mutex);
-        verdict = -1;
+        fit_ok = -1;
         for (int i = 0; i < g_fz_nchecks; ++i)
             if (g_fz_checks[i].dev == dev && g_fz_checks[i].smem == (int)smem && g_fz_checks[i].units == units)
-                verdict = g_fz_checks[i].ok;
-        if (verdict >= 0) return cudaSuccess;
+                fit_ok = g_fz_checks[i].ok;
+        if (fit_ok >= 0) return cudaSuccess;
         if ((int)smem > g_fz_smem_set[dev]) {
             const cudaError_t er = cudaFuncSetAttribute(decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (er != cudaSuccess) return er;
@@ -642,8 +642,8 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t st, unsig
             (void)cudaGetLastError();
             nclusters = 0;
         }
-        verdict = nclusters >= units ? 1 : 0;
-        if (g_fz_nchecks < 32) g_fz_checks[g_fz_nchecks++] = FzCheck{dev, (int)smem, units, verdict};
+        fit_ok = nclusters >= units ? 1 : 0;
+        if (g_fz_nchecks < 32) g_fz_checks[g_fz_nchecks++] = FzCheck{dev, (int)smem, units, fit_ok};
         return cudaSuccess;
     };
     // ring of chunk-pair slots within `budget` bytes of shared memory per CTA (less the static
@@ -658,7 +658,7 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t st, unsig
     // same layer ran ~1.5 us behind the others and held up the whole layer: 16.2 -> 15.5 us per
     // layer at d = 2048, I = 512); more than half of an SM's shared memory keeps a second one
     // out.  Grids with more clusters than fit that way take two CTAs per SM (116736 bytes each).
-    int ring = 0, verdict = 0;
+    int ring = 0, fit_ok = 0;
     size_t smem = 0;
     const int r1 = ring_for(232448);
     if (r1 > 0) {
@@ -667,17 +667,17 @@ cudaError_t launch_decode_fused(const FusedDecodeArgs& a, cudaStream_t st, unsig
 #ifdef MOE_FZ_MIN_SMEM
         if (smem < (size_t)(MOE_FZ_MIN_SMEM)) smem = MOE_FZ_MIN_SMEM;   // tuning builds
 #endif
-        if ((e = fits(smem, verdict)) != cudaSuccess) return e;
+        if ((e = fits(smem, fit_ok)) != cudaSuccess) return e;
         ring = r1;
     }
-    if (!verdict) {
+    if (!fit_ok) {
         const int r2 = ring_for(116736);
         if (r2 == 0) return cudaErrorNotSupported;
         smem = (size_t)r2 * kChunkPairBytes + (size_t)a.d * 2;
-        if ((e = fits(smem, verdict)) != cudaSuccess) return e;
+        if ((e = fits(smem, fit_ok)) != cudaSuccess) return e;
         ring = r2;
     }
-    if (!verdict) return cudaErrorNotSupported;
+    if (!fit_ok) return cudaErrorNotSupported;
     FzParams P{a, NS, ring};
     cfg.dynamicSmemBytes = smem;
     cfg.numAttrs = 2;
